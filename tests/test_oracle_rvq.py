@@ -1,0 +1,116 @@
+"""Pins for the oracle's randomized Hadamard transform and residual VQ."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import rvq as R
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 64])
+def test_sylvester_is_orthogonal_and_symmetric(n):
+    h = R.sylvester(n)
+    assert np.allclose(h @ h, np.eye(n), atol=1e-14)
+    assert np.array_equal(h, h.T)
+    assert np.allclose(np.abs(h), 1 / np.sqrt(n))
+
+
+def test_sylvester_small_explicit():
+    h4 = np.array([[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]]) / 2.0
+    assert np.array_equal(R.sylvester(4), h4)
+
+
+@pytest.mark.parametrize("n", [2, 8, 32, 64])
+def test_fwht_equals_matrix_product(n):
+    v = np.random.default_rng(n).standard_normal((5, n))
+    assert np.allclose(R.fwht(v, axis=1), v @ R.sylvester(n), atol=1e-13)
+    assert np.allclose(R.fwht(v.T, axis=0), (v @ R.sylvester(n)).T, atol=1e-13)
+
+
+def test_rotation_round_trip_and_product_identity():
+    w = synth.rvq_weight(4, 0, 0, 64, 128)
+    so, si = synth.rvq_signs(4, 0, 0, 64, 128)
+    wr = R.rotate_weight(w, so, si)
+    assert np.max(np.abs(R.unrotate_weight(wr, so, si) - w)) < 1e-12
+    # Frobenius norm is preserved by the orthogonal change of basis
+    assert np.isclose(np.linalg.norm(wr), np.linalg.norm(w), rtol=1e-13)
+    # the transform-aware product on the exact rotated weight equals the plain product
+    x = synth.bf16_to_f64(synth.activations_bf16(4, 3, 128))
+    assert np.allclose(R.linear(x, wr, so, si), x @ w.T, rtol=0, atol=1e-12)
+
+
+def test_nearest_lowest_index_ties():
+    cb = np.array([[1.0, 0.0], [-1.0, 0.0], [1.0, 0.0]])
+    u = np.array([[0.0, 0.0], [1.0, 0.1], [0.9, 0.0]])
+    assert R.nearest(u, cb).tolist() == [0, 0, 0]
+    rng = np.random.default_rng(0)
+    u = rng.standard_normal((300, 8))
+    cb = rng.standard_normal((17, 8))
+    brute = [min(range(17), key=lambda j: (float(((u[i] - cb[j]) ** 2).sum()), j)) for i in range(300)]
+    assert R.nearest(u, cb).tolist() == brute
+
+
+def _objective(v, cent):
+    a = R.nearest(v, cent)
+    return float(((v - cent[a]) ** 2).sum())
+
+
+def test_kmeans_objective_non_increasing():
+    v = np.random.default_rng(1).standard_normal((4000, 8))
+    objs = [_objective(v, R.kmeans(v, 32, it, seed=3)) for it in range(0, 8)]
+    assert all(a >= b - 1e-9 for a, b in zip(objs, objs[1:]))
+    assert objs[-1] < objs[0]
+
+
+def test_kmeans_empty_cluster_keeps_centroid():
+    # two far clusters and four centroids initialised from the data: after one
+    # step every centroid is either a member mean or its previous value
+    v = np.concatenate([np.zeros((50, 2)) + [0.0, 0.0], np.zeros((50, 2)) + [10.0, 10.0]])
+    v = v + np.random.default_rng(2).standard_normal(v.shape) * 1e-3
+    c0 = R.kmeans(v, 4, 0, seed=1)
+    c1 = R.kmeans(v, 4, 1, seed=1)
+    a = R.nearest(v, c0)
+    for j in range(4):
+        m = v[a == j]
+        assert np.allclose(c1[j], m.mean(axis=0) if len(m) else c0[j])
+
+
+def test_decode_definition_float32():
+    cb = np.zeros((2, 256, 8), dtype=np.float16)
+    cb[0, 3] = np.float16(0.5)
+    cb[1, 7] = np.float16(-0.125)
+    cb[0, 9] = np.float16(1.0 / 3.0)
+    cb[1, 9] = np.float16(1.0 / 7.0)
+    idx = np.array([[[3, 7], [9, 9]]], dtype=np.uint8)
+    s = np.array([np.float16(0.0213)]).view(np.uint16)
+    w = R.decode(idx, cb.view(np.uint16), s)
+    sf = np.float32(np.float16(0.0213))
+    assert w.dtype == np.float32
+    assert w[0, 0] == sf * (np.float32(0.5) + np.float32(-0.125))
+    assert w[0, 8] == sf * (np.float32(np.float16(1 / 3)) + np.float32(np.float16(1 / 7)))
+
+
+def test_rvq_codec_quality():
+    rng = np.random.default_rng(5)
+    w = rng.normal(0, 0.02, size=(128, 256))
+    so, si = synth.rvq_signs(5, 0, 0, 128, 256)
+    wr = R.rotate_weight(w, so, si)
+    scale = R.row_scale_f16(wr)
+    u = R.normalised_vectors(wr, scale, 8)
+    cb = R.fit_codebooks(u, k=256, iters=10, seed=7)
+    assert np.array_equal(cb, cb.astype(np.float16).astype(np.float64))
+    idx, sc = R.encode(wr, cb)
+    assert np.array_equal(sc, scale)
+    dec = R.decode(idx, cb.astype(np.float16).view(np.uint16), sc).astype(np.float64)
+    rel = np.linalg.norm(dec - wr) / np.linalg.norm(wr)
+    # one stage alone is worse than two
+    i1 = R.nearest(u, cb[0])
+    one = (cb[0][i1].reshape(128, 256) * synth.f16_to_f64(sc)[:, None])
+    rel1 = np.linalg.norm(one - wr) / np.linalg.norm(wr)
+    assert rel < rel1 < 1.0
+    assert rel < 0.45
+
+
+def test_silu_closed_form():
+    assert R.silu(np.array([0.0]))[0] == 0.0
+    assert np.isclose(R.silu(np.array([1.0]))[0], 1.0 / (1.0 + np.exp(-1.0)))
+    assert np.isclose(R.silu(np.array([-20.0]))[0], -20.0 * np.exp(-20.0) / (1 + np.exp(-20.0)))
