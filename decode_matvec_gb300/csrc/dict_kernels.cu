@@ -1,0 +1,803 @@
+// Dictionary-coded ternary path: fused decode-and-multiply kernels for sm_103a.
+//
+// The format is QMoE's (QMoE paper-summary page, "The Fixed-to-Variable
+// Dictionary Code"): 16-bit codewords index a shared 2^16-entry dictionary of
+// runs of 2..28 ternary weights; rows are independent, cut into blocks with
+// start offsets.  QMoE's own kernel (its Listing 1, written for sm_86) gives a
+// whole warp to one codeword at a time and multiplies all 28 lanes.  This
+// design instead gives each lane its own codeword: the lane looks the codeword
+// up in a compact derived table that lists only the run length and the (at
+// most three) nonzero positions and signs, a warp-wide prefix sum of the run
+// lengths places every run in its row, and each lane adds +-x only at its
+// nonzero positions (about 2.4 per codeword instead of 28 multiplies).  The
+// compact table (192 KB) is staged in shared memory for large launches and read
+// through the L1/L2 path for small ones.  Several tokens that share an expert
+// are handled in the same pass (the "inner loop over tokens" the QMoE page
+// proposes for batched experts): activations are staged in shared memory as
+// [column][token] so that one nonzero reads all of its tokens in one access.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "device_common.cuh"
+
+namespace {
+
+__device__ int g_dict_error;
+
+__device__ __forceinline__ void set_error(int code) { atomicCAS(&g_dict_error, 0, code); }
+
+constexpr int kDictA = 2 * QMOE_DICT_ENTRIES;          // bytes of the uint16 plane
+constexpr int kDictBytes = QMOE_COMPACT_BYTES;          // both planes
+constexpr int kSlotEmpty = 63;
+constexpr int kSmemMax = 232448;                        // 227 KB opt-in per block
+constexpr int kXsBudgetSmemDict = kSmemMax - kDictBytes - 1024;
+constexpr int kXsBudgetGlobalDict = 48 * 1024;
+
+struct MatDev {
+    const uint16_t* codes;
+    const uint64_t* code_base;
+    const uint32_t* blk_off;
+    const uint16_t* scale;
+    int count, rows, cols, block, nb;
+};
+
+using qmoe::Job;
+using qmoe::kPlanMaxE;
+
+enum OutMode : int {
+    OUT_PLAIN = 0,     // y[token][row] = s * acc              (fp32 or bf16)
+    OUT_RELU_H = 1,    // h[slot][row] = bf16(relu(s * acc))
+    OUT_GATED = 2,     // y[slot / k][row] = gate[slot] * s * acc   (k == 1 only)
+    OUT_SLOT_F32 = 3,  // o[slot][row] = s * acc  (fp32)
+};
+
+struct GemmArgs {
+    const uint16_t* dictA;       // compact plane A (uint16 per entry)
+    const uint8_t* dictB;        // compact plane B (uint8 per entry)
+    const uint32_t* words;       // canonical entries (for escape entries)
+    MatDev m;
+    const uint16_t* x;           // bf16 rows of `cols` values
+    int x_div;                   // source row of slot s is s / x_div
+    // jobs: either a device table (jobs != nullptr, count in *n_jobs_dev) or
+    // implicit chunks of nt_max tokens over tokens [0, T) of matrix 0
+    const Job* jobs;
+    const int* n_jobs_dev;
+    const int* slots;            // slot list (perm) for table jobs
+    int T_implicit;
+    int nt_max;
+    int rows_per_tile;
+    int row_tiles;
+    int mode;
+    int y_is_f32;
+    void* out;
+    const float* gates;
+};
+
+__device__ __forceinline__ int nt_class(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
+
+// Accumulate +-x[p][0..NT) into acc for one compact-table slot.
+template <int NT>
+__device__ __forceinline__ void apply_slot(int nz, int start, int kcols, float (&acc)[NT],
+                                           const void* xs, bool& bad) {
+    if (nz == kSlotEmpty) return;
+    int p = start + (nz >> 1);
+    if (p >= kcols) {
+        bad = true;
+        return;
+    }
+    float sg = (nz & 1) ? -1.0f : 1.0f;
+    if constexpr (NT == 1) {
+        acc[0] = fmaf(sg, ((const float*)xs)[p], acc[0]);
+    } else if constexpr (NT == 2) {
+        uint32_t w = ((const uint32_t*)xs)[p];
+        acc[0] = fmaf(sg, bf16_lo(w), acc[0]);
+        acc[1] = fmaf(sg, bf16_hi(w), acc[1]);
+    } else if constexpr (NT == 4) {
+        uint2 w = ((const uint2*)xs)[p];
+        acc[0] = fmaf(sg, bf16_lo(w.x), acc[0]);
+        acc[1] = fmaf(sg, bf16_hi(w.x), acc[1]);
+        acc[2] = fmaf(sg, bf16_lo(w.y), acc[2]);
+        acc[3] = fmaf(sg, bf16_hi(w.y), acc[3]);
+    } else {
+        uint4 w = ((const uint4*)xs)[p];
+        acc[0] = fmaf(sg, bf16_lo(w.x), acc[0]);
+        acc[1] = fmaf(sg, bf16_hi(w.x), acc[1]);
+        acc[2] = fmaf(sg, bf16_lo(w.y), acc[2]);
+        acc[3] = fmaf(sg, bf16_hi(w.y), acc[3]);
+        acc[4] = fmaf(sg, bf16_lo(w.z), acc[4]);
+        acc[5] = fmaf(sg, bf16_hi(w.z), acc[5]);
+        acc[6] = fmaf(sg, bf16_lo(w.w), acc[6]);
+        acc[7] = fmaf(sg, bf16_hi(w.w), acc[7]);
+    }
+}
+
+template <bool DICT_SMEM>
+__device__ __forceinline__ void lookup(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB,
+                                       uint32_t code, uint32_t& ea, uint32_t& eb) {
+    if constexpr (DICT_SMEM) {
+        ea = sA[code];
+        eb = sB[code];
+    } else {
+        ea = __ldg(a.dictA + code);
+        eb = __ldg(a.dictB + code);
+    }
+}
+
+// One output row of one matrix for NT staged tokens.  Returns the per-token
+// sums (already reduced across the warp) in acc, valid in every lane.
+template <int NT, bool DICT_SMEM>
+__device__ __forceinline__ void row_dot(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB,
+                                        const uint16_t* codes, uint32_t n, int cols, const void* xs,
+                                        float (&acc)[NT], int lane) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+    int pos = 0;
+    bool bad = false;
+    uint32_t code_next = lane < n ? (uint32_t)__ldg(codes + lane) : 0u;
+    for (uint32_t i = 0; i < n; i += 32) {
+        const uint32_t code = code_next;
+        const bool valid = i + lane < n;
+        if (i + 32 + lane < n) code_next = (uint32_t)__ldg(codes + i + 32 + lane);
+        // lanes past the end of the row: run length 0 and all three slots empty
+        uint32_t ea = (kSlotEmpty << 4) | (kSlotEmpty << 10), eb = kSlotEmpty;
+        if (valid) lookup<DICT_SMEM>(a, sA, sB, code, ea, eb);
+        const int len = (int)(ea & 15u) * 2;
+        const int incl = warp_incl_scan(len, lane);
+        const int start = pos + incl - len;
+        apply_slot<NT>((int)((ea >> 4) & 63u), start, cols, acc, xs, bad);
+        apply_slot<NT>((int)(ea >> 10), start, cols, acc, xs, bad);
+        apply_slot<NT>((int)(eb & 63u), start, cols, acc, xs, bad);
+        if (eb & 64u) {
+            // entry with more than three nonzeros: walk its canonical words
+            const uint32_t w0 = __ldg(a.words + 2 * code), w1 = __ldg(a.words + 2 * code + 1);
+            for (int q = 0; q < len; ++q) {
+                const uint32_t s = ((q < 14 ? w0 : w1) >> (4 + 2 * (q % 14))) & 3u;
+                if (s == 1u || s == 2u) apply_slot<NT>(2 * q + (s == 1u ? 1 : 0), start, cols, acc, xs, bad);
+            }
+        }
+        pos += __shfl_sync(QMOE_FULL_MASK, incl, 31);
+    }
+    if (lane == 0 && (pos != cols)) bad = true;
+    if (__any_sync(QMOE_FULL_MASK, bad) && lane == 0) set_error(QMOE_EFORMAT);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = warp_sum(acc[t]);
+}
+
+__device__ __forceinline__ void job_of(const GemmArgs& a, int j, Job& job) {
+    if (a.jobs) {
+        job = a.jobs[j];
+    } else {
+        job.matrix = 0;
+        job.slot_begin = j * a.nt_max;
+        job.n_tok = min(a.nt_max, a.T_implicit - j * a.nt_max);
+    }
+}
+
+__device__ __forceinline__ int slot_at(const GemmArgs& a, const Job& job, int i) {
+    return a.slots ? a.slots[job.slot_begin + i] : job.slot_begin + i;
+}
+
+template <int NT>
+__device__ void stage_x(const GemmArgs& a, const Job& job, void* xs, int tid, int nthreads) {
+    const int cols = a.m.cols;
+    if constexpr (NT == 1) {
+        const uint16_t* src = a.x + (size_t)(slot_at(a, job, 0) / a.x_div) * cols;
+        float* d = (float*)xs;
+        for (int c = tid; c < cols; c += nthreads) d[c] = bf16_to_f32(src[c]);
+    } else {
+        uint16_t* d = (uint16_t*)xs;
+        for (int t = 0; t < NT; ++t) {
+            if (t < job.n_tok) {
+                const uint16_t* src = a.x + (size_t)(slot_at(a, job, t) / a.x_div) * cols;
+                for (int c = tid; c < cols; c += nthreads) d[c * NT + t] = src[c];
+            } else {
+                for (int c = tid; c < cols; c += nthreads) d[c * NT + t] = 0;
+            }
+        }
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void epilogue(const GemmArgs& a, const Job& job, int row, float s,
+                                         const float (&acc)[NT], int lane) {
+    const int rows = a.m.rows;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (lane == t && t < job.n_tok) {
+            const int slot = slot_at(a, job, t);
+            const float v = s * acc[t];
+            switch (a.mode) {
+                case OUT_PLAIN:
+                    if (a.y_is_f32) ((float*)a.out)[(size_t)slot * rows + row] = v;
+                    else ((uint16_t*)a.out)[(size_t)slot * rows + row] = f32_to_bf16(v);
+                    break;
+                case OUT_RELU_H:
+                    ((uint16_t*)a.out)[(size_t)slot * rows + row] = f32_to_bf16(fmaxf(v, 0.0f));
+                    break;
+                case OUT_GATED: {
+                    const float g = a.gates[slot] * v;
+                    if (a.y_is_f32) ((float*)a.out)[(size_t)slot * rows + row] = g;
+                    else ((uint16_t*)a.out)[(size_t)slot * rows + row] = f32_to_bf16(g);
+                    break;
+                }
+                default:
+                    ((float*)a.out)[(size_t)slot * rows + row] = v;
+                    break;
+            }
+        }
+    }
+}
+
+template <int NT, bool DICT_SMEM>
+__device__ void tile_rows(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const Job& job,
+                          int r0, const void* xs, int warp, int nwarps, int lane) {
+    const MatDev& m = a.m;
+    const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
+    const uint16_t* codes = m.codes + (m.code_base ? m.code_base[job.matrix] : 0ull);
+    const uint16_t* scale = m.scale + (size_t)job.matrix * m.rows;
+    const int r1 = min(m.rows, r0 + a.rows_per_tile);
+    for (int r = r0 + warp; r < r1; r += nwarps) {
+        const uint32_t lo = off[(size_t)r * m.nb], hi = off[(size_t)(r + 1) * m.nb];
+        if (hi < lo) {
+            if (lane == 0) set_error(QMOE_EFORMAT);
+            continue;
+        }
+        float acc[NT];
+        row_dot<NT, DICT_SMEM>(a, sA, sB, codes + lo, hi - lo, m.cols, xs, acc, lane);
+        epilogue<NT>(a, job, r, f16_to_f32(scale[r]), acc, lane);
+    }
+}
+
+template <bool DICT_SMEM>
+__global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int tid = threadIdx.x, nthreads = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+    const uint16_t* sA = nullptr;
+    const uint8_t* sB = nullptr;
+    unsigned char* xs = smem;
+    if constexpr (DICT_SMEM) {
+        const uint4* srcA = (const uint4*)a.dictA;
+        const uint4* srcB = (const uint4*)a.dictB;
+        uint4* dst = (uint4*)smem;
+        for (int i = tid; i < kDictA / 16; i += nthreads) dst[i] = __ldg(srcA + i);
+        for (int i = tid; i < QMOE_DICT_ENTRIES / 16; i += nthreads) dst[kDictA / 16 + i] = __ldg(srcB + i);
+        sA = (const uint16_t*)smem;
+        sB = (const uint8_t*)(smem + kDictA);
+        xs = smem + kDictBytes;
+        __syncthreads();
+    }
+    const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
+    const int n_tiles = n_jobs * a.row_tiles;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        Job job;
+        job_of(a, tile / a.row_tiles, job);
+        const int r0 = (tile % a.row_tiles) * a.rows_per_tile;
+        const int nt = nt_class(job.n_tok);
+        switch (nt) {
+            case 1: stage_x<1>(a, job, xs, tid, nthreads); break;
+            case 2: stage_x<2>(a, job, xs, tid, nthreads); break;
+            case 4: stage_x<4>(a, job, xs, tid, nthreads); break;
+            default: stage_x<8>(a, job, xs, tid, nthreads); break;
+        }
+        __syncthreads();
+        switch (nt) {
+            case 1: tile_rows<1, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
+            case 2: tile_rows<2, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
+            case 4: tile_rows<4, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
+            default: tile_rows<8, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------ decode (test)
+__global__ void decode_dense_kernel(const uint32_t* __restrict__ words, MatDev m, float* __restrict__ out) {
+    const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= m.rows * m.nb) return;
+    const int r = gw / m.nb, b = gw % m.nb;
+    const int c0 = b * m.block, blen = min(m.cols, c0 + m.block) - c0;
+    float* o = out + (size_t)r * m.cols + c0;
+    for (int p = lane; p < blen; p += 32) o[p] = 0.0f;
+    __syncwarp();
+    const uint32_t lo = m.blk_off[(size_t)r * m.nb + b], hi = m.blk_off[(size_t)r * m.nb + b + 1];
+    const float s = f16_to_f32(m.scale[r]);
+    bool bad = hi < lo;
+    int base = 0;
+    for (uint32_t i = lo; i < hi && !bad; i += 32) {
+        const bool valid = i + lane < hi;
+        uint32_t w0 = 0, w1 = 0;
+        int len = 0;
+        if (valid) {
+            const uint32_t code = m.codes[i + lane];
+            w0 = __ldg(words + 2 * code);
+            w1 = __ldg(words + 2 * code + 1);
+            len = 2 * (int)(w0 & 15u);
+            if ((w1 & 15u) != (w0 & 15u) || len == 0) {
+                bad = true;
+                len = 0;
+            }
+        }
+        const int incl = warp_incl_scan(len, lane);
+        const int start = base + incl - len;
+        for (int q = 0; q < len; ++q) {
+            const int p = start + q;
+            const uint32_t sym = ((q < 14 ? w0 : w1) >> (4 + 2 * (q % 14))) & 3u;
+            if (p >= blen || sym == 3u) {
+                bad = true;
+                break;
+            }
+            o[p] = sym == 0u ? 0.0f : (sym == 1u ? -s : s);
+        }
+        base += __shfl_sync(QMOE_FULL_MASK, incl, 31);
+        bad = __any_sync(QMOE_FULL_MASK, bad);
+    }
+    if (base != blen) bad = true;
+    if (bad && lane == 0) set_error(QMOE_EFORMAT);
+}
+
+// ------------------------------------------------------------ router
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                             float* __restrict__ gates) {
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float* row = logits + (size_t)t * E;
+    int chosen[32];
+    float chosen_v[32];
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+        for (int e = lane; e < E; e += 32) {
+            bool taken = false;
+            for (int q = 0; q < j; ++q) taken |= (chosen[q] == e);
+            if (taken) continue;
+            const float v = row[e];
+            if (v > bv || (v == bv && e < bi)) {
+                bv = v;
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(QMOE_FULL_MASK, bv, d);
+            const int oi = __shfl_xor_sync(QMOE_FULL_MASK, bi, d);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        chosen[j] = bi;
+        chosen_v[j] = bv;
+    }
+    const float mx = chosen_v[0];
+    float sum = 0.0f;
+    for (int e = lane; e < E; e += 32) sum += expf(row[e] - mx);
+    sum = warp_sum(sum);
+    if (lane == 0) {
+        for (int j = 0; j < k; ++j) {
+            ids[(size_t)t * k + j] = chosen[j];
+            gates[(size_t)t * k + j] = expf(chosen_v[j] - mx) / sum;
+        }
+    }
+}
+
+// ------------------------------------------------------------ planner
+// One block: histogram, exclusive scan, stable placement (one warp, in slot
+// order) and the job tables of both matrices of the layer.
+constexpr int kPlanThreads = 1024;
+
+__device__ int block_excl_scan(int v, int* sbuf) {
+    // sbuf: at least 32 ints
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int incl = warp_incl_scan(v, lane);
+    if (lane == 31) sbuf[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int s = lane < nw ? sbuf[lane] : 0;
+        const int si = warp_incl_scan(s, lane);
+        sbuf[lane] = si - s;
+    }
+    __syncthreads();
+    const int res = sbuf[warp] + incl - v;
+    __syncthreads();
+    return res;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ids, int n_slots, int E,
+                                                            int nt_a, int nt_b, int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                                            Job* __restrict__ jobs_a, Job* __restrict__ jobs_b,
+                                                            int* __restrict__ n_jobs) {
+    __shared__ int hist[kPlanMaxE];
+    __shared__ int sbuf[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_slots; i += blockDim.x) {
+        const int e = ids[i];
+        if (e < 0 || e >= E) set_error(QMOE_EINVAL);
+        else atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    // exclusive scan of hist in chunks of blockDim
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < E; base += blockDim.x) {
+        const int e = base + tid;
+        const int c = e < E ? hist[e] : 0;
+        const int ex = block_excl_scan(c, sbuf);
+        if (e < E) {
+            counts[e] = c;
+            offsets[e] = carry + ex;
+        }
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry += ex + c;
+        __syncthreads();
+    }
+    if (tid == 0) offsets[E] = carry;
+    __syncthreads();
+    // stable placement: warp 0 walks the slots in order
+    for (int e = tid; e < E; e += blockDim.x) hist[e] = offsets[e];
+    __syncthreads();
+    if (tid < 32) {
+        const int lane = tid;
+        for (int base = 0; base < n_slots; base += 32) {
+            const int i = base + lane;
+            int e = i < n_slots ? ids[i] : -1;
+            if (e >= E) e = -1;
+            const unsigned act = __ballot_sync(QMOE_FULL_MASK, e >= 0);
+            const unsigned same = __match_any_sync(QMOE_FULL_MASK, e);
+            if (e >= 0) {
+                const unsigned lower = same & act & ((1u << lane) - 1u);
+                const int rank = __popc(lower);
+                const int cur = hist[e];
+                perm[cur + rank] = i;
+                __syncwarp(same);
+                if (lower == 0) hist[e] = cur + __popc(same & act);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    if (!jobs_a) return;
+    // job tables: chunks of nt tokens per expert, in expert order
+    for (int which = 0; which < 2; ++which) {
+        const int nt = which == 0 ? nt_a : nt_b;
+        Job* jobs = which == 0 ? jobs_a : jobs_b;
+        if (tid == 0) carry = 0;
+        __syncthreads();
+        for (int base = 0; base < E; base += blockDim.x) {
+            const int e = base + tid;
+            const int c = e < E ? counts[e] : 0;
+            const int nj = (c + nt - 1) / nt;
+            const int ex = block_excl_scan(nj, sbuf);
+            const int first = carry + ex;
+            for (int q = 0; q < nj; ++q) {
+                Job jb;
+                jb.matrix = e;
+                jb.slot_begin = offsets[e] + q * nt;
+                jb.n_tok = min(nt, c - q * nt);
+                jb.pad = 0;
+                jobs[first + q] = jb;
+            }
+            __syncthreads();
+            if (tid == blockDim.x - 1) carry += ex + nj;
+            __syncthreads();
+        }
+        if (tid == 0) n_jobs[which] = carry;
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------ combine
+__global__ void combine_kernel(const float* __restrict__ o, const float* __restrict__ gates, int T, int k, int d,
+                               void* __restrict__ y, int y_is_f32) {
+    const size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if (i >= (size_t)T * d) return;
+    const size_t t = i / d, c = i % d;
+    float acc = 0.0f;
+    for (int j = 0; j < k; ++j) acc = fmaf(gates[t * k + j], o[(t * k + j) * d + c], acc);
+    if (y_is_f32) ((float*)y)[i] = acc;
+    else ((uint16_t*)y)[i] = f32_to_bf16(acc);
+}
+
+// ------------------------------------------------------------ host side
+int g_sm_count[64];
+
+int nt_max_for(int cols, int budget) {
+    for (int nt = 8; nt >= 2; nt >>= 1)
+        if (cols * nt * 2 <= budget) return nt;
+    return cols * 4 <= budget ? 1 : 0;
+}
+
+size_t xs_bytes(int cols, int nt_max) { return nt_max == 1 ? (size_t)cols * 4 : (size_t)cols * nt_max * 2; }
+
+bool valid_set(const qmoe_matrix_set* s) {
+    return s && s->codes && s->blk_off && s->scale_f16 && s->count >= 1 && s->rows >= 1 && s->cols >= 2 &&
+           (s->cols % 2) == 0 && s->block >= 2 && (s->block % 2) == 0 && (s->count == 1 || s->code_base);
+}
+
+MatDev to_dev(const qmoe_matrix_set* s) {
+    MatDev m;
+    m.codes = s->codes;
+    m.code_base = s->code_base;
+    m.blk_off = s->blk_off;
+    m.scale = s->scale_f16;
+    m.count = s->count;
+    m.rows = s->rows;
+    m.cols = s->cols;
+    m.block = s->block;
+    m.nb = (s->cols + s->block - 1) / s->block;
+    return m;
+}
+
+int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, cudaStream_t st, int grid_hint) {
+    const int sms = qmoe::sm_count();
+    if (dict_smem) {
+        const size_t smem = kDictBytes + xs_bytes(a.m.cols, nt_max);
+        int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<true>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
+                                  "cudaFuncSetAttribute");
+        if (rc) return rc;
+        a.rows_per_tile = 128;
+        a.row_tiles = (a.m.rows + 127) / 128;
+        dict_gemm_kernel<true><<<sms, 512, smem, st>>>(a);
+    } else {
+        const size_t smem = xs_bytes(a.m.cols, nt_max);
+        int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<false>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
+                                  "cudaFuncSetAttribute");
+        if (rc) return rc;
+        a.rows_per_tile = 8;
+        a.row_tiles = (a.m.rows + 7) / 8;
+        int grid = grid_hint > 0 ? std::min(grid_hint, sms * 8) : sms * 4;
+        dict_gemm_kernel<false><<<std::max(grid, 1), 256, smem, st>>>(a);
+    }
+    return qmoe::launch_check("dict_gemm_kernel");
+}
+
+}  // namespace
+
+namespace qmoe {
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 148;
+    }
+    return g_sm_count[dev];
+}
+
+int launch_plan(const int32_t* ids, int n_slots, int E, int nt_a, int nt_b, int32_t* counts, int32_t* offsets,
+                int32_t* perm, Job* jobs_a, Job* jobs_b, int* n_jobs, cudaStream_t st) {
+    plan_kernel<<<1, kPlanThreads, 0, st>>>(ids, n_slots, E, nt_a, nt_b, counts, offsets, perm, jobs_a, jobs_b, n_jobs);
+    return launch_check("plan_kernel");
+}
+
+static cudaEvent_t g_phase[8];
+static int g_n_phase = 0;
+
+void phase_event(int i, cudaStream_t st) {
+    if (i < g_n_phase) cudaEventRecord(g_phase[i], st);
+}
+
+int dict_take_error() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dict_error, sizeof(int)) != cudaSuccess) return QMOE_ECUDA;
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_dict_error, &z, sizeof(int)) != cudaSuccess) return QMOE_ECUDA;
+    return v;
+}
+
+}  // namespace qmoe
+
+using qmoe::fail;
+
+extern "C" int qmoe_decode_dense(const qmoe_dict* dict, const qmoe_matrix_set* mat, float* w_out, void* stream) {
+    qmoe::clear_error();
+    if (!dict || !dict->words || !w_out || !valid_set(mat) || mat->count != 1)
+        return fail(QMOE_EINVAL, "qmoe_decode_dense: bad arguments (count must be 1)");
+    MatDev m = to_dev(mat);
+    const long long warps = (long long)m.rows * m.nb;
+    const int threads = 256;
+    const long long blocks = (warps * 32 + threads - 1) / threads;
+    decode_dense_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(dict->words, m, w_out);
+    return qmoe::launch_check("qmoe_decode_dense");
+}
+
+extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* mat, const void* x_bf16, int T,
+                                  void* y, int y_is_f32, void* stream) {
+    qmoe::clear_error();
+    if (!dict || !dict->words || !dict->compact || !valid_set(mat) || mat->count != 1)
+        return fail(QMOE_EINVAL, "qmoe_expert_matvec: bad dictionary or matrix (count must be 1)");
+    if (T < 0) return fail(QMOE_EINVAL, "qmoe_expert_matvec: T < 0");
+    if (T == 0) return QMOE_OK;
+    if (!x_bf16 || !y) return fail(QMOE_EINVAL, "qmoe_expert_matvec: NULL x or y");
+    const int nt_max = nt_max_for(mat->cols, kXsBudgetGlobalDict);
+    if (!nt_max) return fail(QMOE_EUNSUPPORTED, "qmoe_expert_matvec: cols too large");
+    GemmArgs a{};
+    a.dictA = (const uint16_t*)dict->compact;
+    a.dictB = (const uint8_t*)dict->compact + kDictA;
+    a.words = dict->words;
+    a.m = to_dev(mat);
+    a.x = (const uint16_t*)x_bf16;
+    a.x_div = 1;
+    a.jobs = nullptr;
+    a.slots = nullptr;
+    a.T_implicit = T;
+    a.nt_max = nt_max;
+    a.mode = OUT_PLAIN;
+    a.y_is_f32 = y_is_f32 ? 1 : 0;
+    a.out = y;
+    const int jobs = (T + nt_max - 1) / nt_max;
+    const int tiles = jobs * ((mat->rows + 7) / 8);
+    return launch_gemm(a, false, nt_max, (cudaStream_t)stream, tiles);
+}
+
+extern "C" int qmoe_route(const float* logits, int T, int E, int k, int32_t* ids, float* gates, void* stream) {
+    qmoe::clear_error();
+    if (T < 0 || E < 1 || E > kPlanMaxE || k < 1 || k > E || k > 32)
+        return fail(QMOE_EINVAL, "qmoe_route: need 1 <= k <= min(E, 32), E <= 8192, T >= 0");
+    if (T == 0) return QMOE_OK;
+    if (!logits || !ids || !gates) return fail(QMOE_EINVAL, "qmoe_route: NULL pointer");
+    const int threads = 256;
+    const long long blocks = ((long long)T * 32 + threads - 1) / threads;
+    route_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
+    return qmoe::launch_check("qmoe_route");
+}
+
+namespace {
+struct MoeWs {
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    Job* jobs_a;
+    Job* jobs_b;
+    int* n_jobs;
+    uint16_t* h;
+    float* o;
+    size_t bytes;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+MoeWs moe_ws_layout(void* base, int E, int d_model, int d_ff, int T, int k) {
+    MoeWs w{};
+    size_t off = 0;
+    const size_t slots = (size_t)T * k;
+    auto take = [&](size_t bytes) {
+        void* p = base ? (void*)((char*)base + off) : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    w.counts = (int32_t*)take(sizeof(int32_t) * E);
+    w.offsets = (int32_t*)take(sizeof(int32_t) * (E + 1));
+    w.perm = (int32_t*)take(sizeof(int32_t) * std::max<size_t>(slots, 1));
+    w.jobs_a = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
+    w.jobs_b = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
+    w.n_jobs = (int*)take(sizeof(int) * 2);
+    w.h = (uint16_t*)take(sizeof(uint16_t) * slots * d_ff);
+    w.o = k > 1 ? (float*)take(sizeof(float) * slots * d_model) : nullptr;
+    w.bytes = off;
+    return w;
+}
+}  // namespace
+
+extern "C" int qmoe_bucketise(const int32_t* ids, int T, int k, int E, int32_t* counts, int32_t* offsets,
+                              int32_t* perm, void* stream) {
+    qmoe::clear_error();
+    if (T < 0 || k < 1 || E < 1 || E > kPlanMaxE) return fail(QMOE_EINVAL, "qmoe_bucketise: bad sizes");
+    if (!counts || !offsets || (T > 0 && (!ids || !perm))) return fail(QMOE_EINVAL, "qmoe_bucketise: NULL pointer");
+    return qmoe::launch_plan(ids, T * k, E, 1, 1, counts, offsets, perm, nullptr, nullptr, nullptr,
+                             (cudaStream_t)stream);
+}
+
+extern "C" int qmoe_moe_layer_ws_size(int E, int d_model, int d_ff, int T, int k, size_t* bytes) {
+    qmoe::clear_error();
+    if (!bytes || E < 1 || E > kPlanMaxE || d_model < 2 || d_ff < 2 || T < 0 || k < 1 || k > E)
+        return fail(QMOE_EINVAL, "qmoe_moe_layer_ws_size: bad sizes");
+    *bytes = moe_ws_layout(nullptr, E, d_model, d_ff, T, k).bytes;
+    return QMOE_OK;
+}
+
+extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, const qmoe_matrix_set* wo,
+                              const void* x_bf16, int T, int k, const int32_t* ids, const float* gates, void* y,
+                              int y_is_f32, void* workspace, size_t ws_bytes, void* stream) {
+    qmoe::clear_error();
+    if (!dict || !dict->words || !dict->compact || !valid_set(wi) || !valid_set(wo))
+        return fail(QMOE_EINVAL, "qmoe_moe_layer: bad dictionary or matrix sets");
+    const int E = wi->count, d_model = wi->cols, d_ff = wi->rows;
+    if (wo->count != E || wo->rows != d_model || wo->cols != d_ff)
+        return fail(QMOE_EINVAL, "qmoe_moe_layer: wo must be d_model x d_ff with the same expert count as wi");
+    if (E > kPlanMaxE || T < 0 || k < 1 || k > E) return fail(QMOE_EINVAL, "qmoe_moe_layer: bad E, T or k");
+    if (T == 0) return QMOE_OK;
+    if (!x_bf16 || !ids || !gates || !y || !workspace) return fail(QMOE_EINVAL, "qmoe_moe_layer: NULL pointer");
+    MoeWs w = moe_ws_layout(workspace, E, d_model, d_ff, T, k);
+    if (ws_bytes < w.bytes) return fail(QMOE_ECAPACITY, "qmoe_moe_layer: workspace too small");
+    const long long slots = (long long)T * k;
+    const bool big = slots >= 16;
+    const int budget = big ? kXsBudgetSmemDict : kXsBudgetGlobalDict;
+    const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
+    if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
+    cudaStream_t st = (cudaStream_t)stream;
+    qmoe::phase_event(0, st);
+    int rc = qmoe::launch_plan(ids, (int)slots, E, nt_wi, nt_wo, w.counts, w.offsets, w.perm, w.jobs_a, w.jobs_b,
+                               w.n_jobs, st);
+    if (rc) return rc;
+    qmoe::phase_event(1, st);
+    GemmArgs a{};
+    a.dictA = (const uint16_t*)dict->compact;
+    a.dictB = (const uint8_t*)dict->compact + kDictA;
+    a.words = dict->words;
+    a.slots = w.perm;
+    a.T_implicit = 0;
+    a.y_is_f32 = y_is_f32 ? 1 : 0;
+    a.gates = gates;
+    // wi: h[slot] = bf16(relu(Wi x[slot / k]))
+    a.m = to_dev(wi);
+    a.x = (const uint16_t*)x_bf16;
+    a.x_div = k;
+    a.jobs = w.jobs_a;
+    a.n_jobs_dev = w.n_jobs;
+    a.nt_max = nt_wi;
+    a.mode = OUT_RELU_H;
+    a.out = w.h;
+    rc = launch_gemm(a, big, nt_wi, st, (int)std::min<long long>(slots * ((d_ff + 7) / 8), 1 << 20));
+    if (rc) return rc;
+    qmoe::phase_event(2, st);
+    // wo: o[slot] = Wo h[slot]; gated straight into y when k == 1
+    a.m = to_dev(wo);
+    a.x = w.h;
+    a.x_div = 1;
+    a.jobs = w.jobs_b;
+    a.n_jobs_dev = w.n_jobs + 1;
+    a.nt_max = nt_wo;
+    a.mode = k == 1 ? OUT_GATED : OUT_SLOT_F32;
+    a.out = k == 1 ? y : (void*)w.o;
+    rc = launch_gemm(a, big, nt_wo, st, (int)std::min<long long>(slots * ((d_model + 7) / 8), 1 << 20));
+    if (rc) return rc;
+    qmoe::phase_event(3, st);
+    if (k > 1) {
+        const size_t n = (size_t)T * d_model;
+        combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(w.o, gates, T, k, d_model, y, y_is_f32 ? 1 : 0);
+        rc = qmoe::launch_check("combine_kernel");
+    }
+    qmoe::phase_event(4, st);
+    return rc;
+}
+
+extern "C" int qmoe_set_phase_events(void* const* events, int n) {
+    qmoe::clear_error();
+    if (!events || n == 0) {
+        qmoe::g_n_phase = 0;
+        return QMOE_OK;
+    }
+    if (n < 6 || n > 8) return fail(QMOE_EINVAL, "qmoe_set_phase_events: need 6..8 events");
+    for (int i = 0; i < n; ++i) qmoe::g_phase[i] = (cudaEvent_t)events[i];
+    qmoe::g_n_phase = n;
+    return QMOE_OK;
+}
+
+extern "C" int qmoe_check_status(void* stream) {
+    qmoe::clear_error();
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return qmoe::cuda_check(e, "qmoe_check_status");
+    const int a = qmoe::dict_take_error();
+    const int b = qmoe::rvq_take_error();
+    if (a == QMOE_ECUDA || b == QMOE_ECUDA) return fail(QMOE_ECUDA, "qmoe_check_status: reading the error word failed");
+    if (a) return fail(a, "device reported an error (dictionary kernels)");
+    if (b) return fail(b, "device reported an error (RVQ kernels)");
+    return QMOE_OK;
+}

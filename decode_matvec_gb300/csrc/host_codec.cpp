@@ -1,0 +1,393 @@
+// Host-side codec of the decode-and-multiply library: dictionary generation
+// (QMoE page, Algorithm 1), the greedy longest-match packer ("Encoding
+// (compression time)"), the kernel-private compact dictionary and the RVQ
+// encoder ("Quantization as Cache Amplification", section "Codec").
+//
+// Built with -ffp-contract=off: the float64 arithmetic of the RVQ encoder must
+// round exactly as written so that independent exact encoders agree bit for bit.
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "qmoe.h"
+#include "host_common.h"
+
+namespace qmoe {
+
+static thread_local std::string g_last_error;
+
+int fail(int status, const std::string& msg) {
+    g_last_error = msg;
+    return status;
+}
+
+const char* last_error() { return g_last_error.c_str(); }
+void clear_error() { g_last_error.clear(); }
+
+}  // namespace qmoe
+
+using qmoe::fail;
+
+extern "C" const char* qmoe_last_error(void) { return qmoe::last_error(); }
+
+// ---------------------------------------------------------------------------
+// Algorithm 1
+// ---------------------------------------------------------------------------
+namespace {
+
+// A sequence of up to 28 ternary symbols.  `key` holds symbol i at bits
+// [55-2i : 54-2i] (first symbol most significant), zero-padded, so comparing
+// (key, len) orders sequences lexicographically with a prefix first.
+struct Seq {
+    double prio;
+    uint64_t key;
+    int len;
+    int n0;
+};
+
+struct HeapLess {
+    // std::priority_queue pops the "largest": the highest priority, then the
+    // lexicographically smallest sequence.
+    bool operator()(const Seq& a, const Seq& b) const {
+        if (a.prio != b.prio) return a.prio < b.prio;
+        if (a.key != b.key) return a.key > b.key;
+        return a.len > b.len;
+    }
+};
+
+inline int sym_at(uint64_t key, int i) { return (int)((key >> (54 - 2 * i)) & 3u); }
+
+}  // namespace
+
+extern "C" int qmoe_encode_dictionary(const int8_t* symbols, size_t n, double p0,
+                                      uint32_t* dict_words, double* p0_used) {
+    qmoe::clear_error();
+    if (!dict_words) return fail(QMOE_EINVAL, "qmoe_encode_dictionary: dict_words is NULL");
+    if (symbols) {
+        if (n == 0) return fail(QMOE_EINVAL, "qmoe_encode_dictionary: no symbols given");
+        size_t zeros = 0;
+        for (size_t i = 0; i < n; ++i) {
+            int8_t v = symbols[i];
+            if (v < -1 || v > 1) return fail(QMOE_EINVAL, "qmoe_encode_dictionary: symbol outside {-1,0,1}");
+            zeros += (v == 0);
+        }
+        p0 = (double)zeros / (double)n;
+    }
+    if (!(p0 > 0.0 && p0 < 1.0)) return fail(QMOE_EINVAL, "qmoe_encode_dictionary: p0 must lie in (0,1)");
+    if (p0_used) *p0_used = p0;
+
+    const double lp0 = std::log(p0);
+    const double lq = std::log((1.0 - p0) / 2.0);
+    std::priority_queue<Seq, std::vector<Seq>, HeapLess> heap;
+    heap.push(Seq{-0.0, 0, 0, 0});
+    int count = 0;
+    while (count < QMOE_DICT_ENTRIES) {
+        Seq s = heap.top();
+        heap.pop();
+        if (s.len >= 1 && s.len <= QMOE_MAX_RUN) {
+            uint32_t pairs = (uint32_t)(s.len / 2);
+            uint32_t w[2] = {pairs, pairs};
+            for (int i = 0; i < s.len; ++i)
+                w[i / 14] |= (uint32_t)sym_at(s.key, i) << (4 + 2 * (i % 14));
+            dict_words[2 * count] = w[0];
+            dict_words[2 * count + 1] = w[1];
+            ++count;
+        }
+        if (s.len < QMOE_MAX_RUN) {
+            for (int t1 = 0; t1 < 3; ++t1)
+                for (int t2 = 0; t2 < 3; ++t2) {
+                    Seq c;
+                    c.len = s.len + 2;
+                    c.key = s.key | ((uint64_t)t1 << (54 - 2 * s.len)) | ((uint64_t)t2 << (52 - 2 * s.len));
+                    c.n0 = s.n0 + (t1 == 0) + (t2 == 0);
+                    // recomputed from the counts, as the priority of equal-count
+                    // sequences must tie exactly
+                    c.prio = (double)c.n0 * lp0 + (double)(c.len - c.n0) * lq;
+                    heap.push(c);
+                }
+        }
+    }
+    return QMOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Packer: a trie over ternary pairs (9 children per node)
+// ---------------------------------------------------------------------------
+namespace {
+
+struct Trie {
+    std::vector<int32_t> child;   // [node*9 + pair]
+    std::vector<int32_t> code;    // codeword of the node's sequence, or -1
+    uint64_t hash = 0;
+    bool ok = false;
+};
+
+uint64_t fnv1a(const uint32_t* w, size_t n) {
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < n; ++i) {
+        h ^= w[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+int build_trie(const uint32_t* words, Trie& t) {
+    t.child.assign(9, -1);
+    t.code.assign(1, -1);
+    for (int e = 0; e < QMOE_DICT_ENTRIES; ++e) {
+        uint32_t w0 = words[2 * e], w1 = words[2 * e + 1];
+        int pairs = (int)(w0 & 15u);
+        if ((w1 & 15u) != (uint32_t)pairs || pairs < 1 || pairs > 14)
+            return fail(QMOE_EFORMAT, "qmoe_pack: dictionary entry with a bad pair count");
+        int node = 0;
+        for (int p = 0; p < pairs; ++p) {
+            int i0 = 2 * p, i1 = 2 * p + 1;
+            uint32_t a = ((i0 < 14 ? w0 : w1) >> (4 + 2 * (i0 % 14))) & 3u;
+            uint32_t b = ((i1 < 14 ? w0 : w1) >> (4 + 2 * (i1 % 14))) & 3u;
+            if (a == 3 || b == 3) return fail(QMOE_EFORMAT, "qmoe_pack: dictionary symbol 3");
+            int pr = (int)(a * 3 + b);
+            int nxt = t.child[(size_t)node * 9 + pr];
+            if (nxt < 0) {
+                nxt = (int)t.code.size();
+                t.code.push_back(-1);
+                t.child.insert(t.child.end(), 9, -1);
+                t.child[(size_t)node * 9 + pr] = nxt;
+            }
+            node = nxt;
+        }
+        if (t.code[node] < 0) t.code[node] = e;   // first (most probable) code wins
+    }
+    t.ok = true;
+    return QMOE_OK;
+}
+
+std::mutex g_trie_mu;
+std::shared_ptr<Trie> g_trie;
+
+int get_trie(const uint32_t* words, std::shared_ptr<Trie>& out) {
+    uint64_t h = fnv1a(words, QMOE_DICT_WORDS);
+    std::lock_guard<std::mutex> lk(g_trie_mu);
+    if (g_trie && g_trie->ok && g_trie->hash == h) {
+        out = g_trie;
+        return QMOE_OK;
+    }
+    auto t = std::make_shared<Trie>();
+    int st = build_trie(words, *t);
+    if (st) return st;
+    t->hash = h;
+    g_trie = t;
+    out = t;
+    return QMOE_OK;
+}
+
+}  // namespace
+
+extern "C" int qmoe_pack(const int8_t* tern, int rows, int cols, int block,
+                         const uint32_t* dict_words, uint16_t* codes, size_t codes_cap,
+                         size_t* n_codes, uint32_t* blk_off) {
+    qmoe::clear_error();
+    if (!tern && (size_t)rows * (size_t)cols != 0) return fail(QMOE_EINVAL, "qmoe_pack: tern is NULL");
+    if (!dict_words || !n_codes) return fail(QMOE_EINVAL, "qmoe_pack: NULL argument");
+    if (rows < 0 || cols <= 0 || (cols & 1) || block <= 0 || (block & 1))
+        return fail(QMOE_EINVAL, "qmoe_pack: rows >= 0, cols > 0 even and block > 0 even required");
+    if (codes && !blk_off) return fail(QMOE_EINVAL, "qmoe_pack: blk_off is NULL");
+    std::shared_ptr<Trie> trie;
+    int st = get_trie(dict_words, trie);
+    if (st) return st;
+    const int nb = (cols + block - 1) / block;
+    size_t count = 0;
+    bool overflow = false;
+    for (int r = 0; r < rows; ++r) {
+        const int8_t* row = tern + (size_t)r * cols;
+        for (int b = 0; b < nb; ++b) {
+            if (blk_off && !overflow) blk_off[(size_t)r * nb + b] = (uint32_t)count;
+            const int c_end = std::min(cols, (b + 1) * block);
+            int pos = b * block;
+            while (pos < c_end) {
+                int node = 0, best = -1, best_len = 0;
+                for (int p = 0; p < 14 && pos + 2 * p + 2 <= c_end; ++p) {
+                    int8_t va = row[pos + 2 * p], vb = row[pos + 2 * p + 1];
+                    if (va < -1 || va > 1 || vb < -1 || vb > 1)
+                        return fail(QMOE_EINVAL, "qmoe_pack: weight outside {-1,0,1}");
+                    int a = va == 0 ? 0 : (va < 0 ? 1 : 2);
+                    int bb = vb == 0 ? 0 : (vb < 0 ? 1 : 2);
+                    int nxt = trie->child[(size_t)node * 9 + a * 3 + bb];
+                    if (nxt < 0) break;
+                    node = nxt;
+                    if (trie->code[node] >= 0) {
+                        best = trie->code[node];
+                        best_len = 2 * p + 2;
+                    }
+                }
+                if (best < 0) return fail(QMOE_EFORMAT, "qmoe_pack: the dictionary cannot express a pair");
+                if (codes) {
+                    if (count < codes_cap) codes[count] = (uint16_t)best;
+                    else overflow = true;
+                }
+                ++count;
+                pos += best_len;
+            }
+        }
+    }
+    if (blk_off && !overflow) blk_off[(size_t)rows * nb] = (uint32_t)count;
+    *n_codes = count;
+    if (count > 0xFFFFFFFFull && blk_off) return fail(QMOE_EINVAL, "qmoe_pack: more than 2^32 codewords in one matrix");
+    if (codes && overflow) return fail(QMOE_ECAPACITY, "qmoe_pack: codes buffer too small");
+    return QMOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Compact dictionary: uint16 plane [65536] then uint8 plane [65536]
+//   plane A: [3:0] pair count, [9:4] slot 0, [15:10] slot 1
+//   plane B: [5:0] slot 2, [6] escape (more than three nonzeros)
+//   slot = 2*position + (1 if the weight is w_min), 63 = empty
+// ---------------------------------------------------------------------------
+extern "C" int qmoe_dict_compact(const uint32_t* dict_words, void* compact) {
+    qmoe::clear_error();
+    if (!dict_words || !compact) return fail(QMOE_EINVAL, "qmoe_dict_compact: NULL argument");
+    uint16_t* pa = (uint16_t*)compact;
+    uint8_t* pb = (uint8_t*)compact + 2 * QMOE_DICT_ENTRIES;
+    for (int e = 0; e < QMOE_DICT_ENTRIES; ++e) {
+        uint32_t w0 = dict_words[2 * e], w1 = dict_words[2 * e + 1];
+        uint32_t pairs = w0 & 15u;
+        if ((w1 & 15u) != pairs || pairs < 1 || pairs > 14)
+            return fail(QMOE_EFORMAT, "qmoe_dict_compact: bad pair count");
+        int slots[3] = {63, 63, 63};
+        int nnz = 0;
+        for (int i = 0; i < 28; ++i) {
+            uint32_t s = ((i < 14 ? w0 : w1) >> (4 + 2 * (i % 14))) & 3u;
+            if (s == 3) return fail(QMOE_EFORMAT, "qmoe_dict_compact: symbol 3");
+            if (i >= (int)(2 * pairs)) {
+                if (s) return fail(QMOE_EFORMAT, "qmoe_dict_compact: nonzero symbol in an unused field");
+                continue;
+            }
+            if (s) {
+                if (nnz < 3) slots[nnz] = 2 * i + (s == 1 ? 1 : 0);
+                ++nnz;
+            }
+        }
+        uint32_t esc = nnz > 3 ? 1u : 0u;
+        if (esc) slots[0] = slots[1] = slots[2] = 63;
+        pa[e] = (uint16_t)(pairs | ((uint32_t)slots[0] << 4) | ((uint32_t)slots[1] << 10));
+        pb[e] = (uint8_t)((uint32_t)slots[2] | (esc << 6));
+    }
+    return QMOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// RVQ encoder
+// ---------------------------------------------------------------------------
+namespace {
+
+double half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1, ex = (h >> 10) & 31, man = h & 1023;
+    double v;
+    if (ex == 0) v = std::ldexp((double)man, -24);
+    else if (ex == 31) v = man ? NAN : INFINITY;
+    else v = std::ldexp((double)(man | 1024), ex - 25);
+    return sign ? -v : v;
+}
+
+// float64 -> IEEE binary16, round to nearest even (finite, non-NaN inputs).
+uint16_t double_to_half(double v) {
+    uint16_t sign = std::signbit(v) ? 0x8000 : 0;
+    double a = std::fabs(v);
+    if (a == 0.0) return sign;
+    if (a >= 65520.0) return sign | 0x7C00;   // rounds to infinity
+    int e;
+    std::frexp(a, &e);                          // a = m * 2^e, m in [0.5, 1)
+    int ex = std::max(e, -13);                  // subnormal quantum 2^-24
+    double q = std::nearbyint(std::ldexp(a, 11 - ex));   // 11 significant bits
+    double r = std::ldexp(q, ex - 11);
+    // re-encode r (exactly representable in binary16)
+    int e2;
+    std::frexp(r, &e2);
+    if (e2 <= -14) return sign | (uint16_t)std::ldexp(r, 24);              // subnormal
+    uint16_t man = (uint16_t)(std::ldexp(r, 11 - e2) - 1024.0);
+    return sign | (uint16_t)((e2 + 14) << 10) | man;
+}
+
+void fwht_strided(double* a, int n, size_t stride) {
+    for (int h = 1; h < n; h *= 2)
+        for (int i = 0; i < n; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                double x = a[(size_t)j * stride], y = a[(size_t)(j + h) * stride];
+                a[(size_t)j * stride] = x + y;
+                a[(size_t)(j + h) * stride] = x - y;
+            }
+    double s = std::sqrt((double)n);
+    for (int i = 0; i < n; ++i) a[(size_t)i * stride] = a[(size_t)i * stride] / s;
+}
+
+int nearest8(const double* u, const double* cb) {
+    int best = 0;
+    double bestd = INFINITY;
+    for (int j = 0; j < QMOE_RVQ_CODES; ++j) {
+        const double* c = cb + j * 8;
+        double d = 0.0;
+        int k = 0;
+        for (; k < 8; ++k) {
+            double diff = u[k] - c[k];
+            d = d + diff * diff;
+            if (d > bestd) break;     // partial sums of squares only grow: cannot win
+        }
+        if (k == 8 && d < bestd) {
+            bestd = d;
+            best = j;
+        }
+    }
+    return best;
+}
+
+bool pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+}  // namespace
+
+extern "C" int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_out,
+                        const int8_t* sign_in, const uint16_t* codebooks, uint8_t* idx,
+                        uint16_t* scale_f16) {
+    qmoe::clear_error();
+    if (!w || !sign_out || !sign_in || !codebooks || !idx || !scale_f16)
+        return fail(QMOE_EINVAL, "rvq_pack: NULL argument");
+    if (!pow2(rows) || !pow2(cols) || cols % 8 || rows > 8192 || cols > 8192)
+        return fail(QMOE_EINVAL, "rvq_pack: rows and cols must be powers of two in [8, 8192]");
+    std::vector<double> a((size_t)rows * cols);
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            if (std::abs(sign_out[r]) != 1 || std::abs(sign_in[c]) != 1)
+                return fail(QMOE_EINVAL, "rvq_pack: signs must be +1 or -1");
+            a[(size_t)r * cols + c] = w[(size_t)r * cols + c] * (double)sign_out[r] * (double)sign_in[c];
+        }
+    for (int c = 0; c < cols; ++c) fwht_strided(a.data() + c, rows, (size_t)cols);
+    for (int r = 0; r < rows; ++r) fwht_strided(a.data() + (size_t)r * cols, cols, 1);
+    double cb[2][QMOE_RVQ_CODES * 8];
+    for (int s = 0; s < 2; ++s)
+        for (int i = 0; i < QMOE_RVQ_CODES * 8; ++i) cb[s][i] = half_to_double(codebooks[s * QMOE_RVQ_CODES * 8 + i]);
+    for (int r = 0; r < rows; ++r) {
+        const double* row = a.data() + (size_t)r * cols;
+        double sum = 0.0;
+        for (int c = 0; c < cols; ++c) sum = sum + row[c] * row[c];
+        uint16_t sh = double_to_half(std::sqrt(sum / (double)cols));
+        double s = half_to_double(sh);
+        if (s == 0.0) return fail(QMOE_EINVAL, "rvq_pack: a row's scale rounds to zero");
+        scale_f16[r] = sh;
+        for (int v = 0; v < cols / 8; ++v) {
+            double u[8], res[8];
+            for (int k = 0; k < 8; ++k) u[k] = row[v * 8 + k] / s;
+            int i1 = nearest8(u, cb[0]);
+            for (int k = 0; k < 8; ++k) res[k] = u[k] - cb[0][i1 * 8 + k];
+            int i2 = nearest8(res, cb[1]);
+            idx[((size_t)r * (cols / 8) + v) * 2] = (uint8_t)i1;
+            idx[((size_t)r * (cols / 8) + v) * 2 + 1] = (uint8_t)i2;
+        }
+    }
+    return QMOE_OK;
+}

@@ -122,8 +122,15 @@ def f16_round(a: np.ndarray) -> np.ndarray:
 
 
 def row_scale_f16(wr: np.ndarray) -> np.ndarray:
-    """Per-row fp16 RMS scale bits of the rotated weight."""
-    rms = np.sqrt(np.mean(np.asarray(wr, np.float64) ** 2, axis=1))
+    """Per-row fp16 RMS scale bits of the rotated weight.
+
+    The sum of squares is taken left to right (cumulative sum), then divided by
+    the row length; reading of "fp16 per-row RMS scale" ([QCA] "Residual vector
+    quantization") with a fixed summation order so that any exact encoder can
+    reproduce the scale bit for bit.
+    """
+    sq = np.asarray(wr, np.float64) ** 2
+    rms = np.sqrt(np.cumsum(sq, axis=1)[:, -1] / wr.shape[1])
     return rms.astype(np.float16).view(np.uint16)
 
 

@@ -1,0 +1,137 @@
+"""The C-ABI library without a GPU: exported symbols and the host codec against the oracle."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import codec as C
+from oracle import dictionary as D
+from oracle import rvq as R
+
+Q = pytest.importorskip("decode_matvec_gb300")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "qmoe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared_functions()
+    assert len(names) >= 17
+    out = subprocess.run(["nm", "-D", "--defined-only", Q.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    for n in names:
+        assert n in exported, n
+        assert getattr(Q.lib(), n) is not None
+    assert sorted(Q.EXPORTED) == names
+
+
+@pytest.mark.parametrize("p0", [0.857, 0.87, 0.886, 0.89, 0.5])
+def test_dictionary_matches_oracle(p0):
+    words, used = Q.qmoe_encode_dictionary(p0)
+    assert used == p0
+    assert np.array_equal(words, D.build(p0))
+
+
+def test_dictionary_from_measured_symbols():
+    tern = synth.ternary_matrix(0, 0, 0, 64, 512, 0.89)
+    words, used = Q.qmoe_encode_dictionary(symbols=tern)
+    assert used == D.measured_p0(tern)
+    assert np.array_equal(words, D.build(used))
+
+
+def test_dictionary_rejects_bad_p0():
+    for bad in (0.0, 1.0, -0.5, 2.0):
+        with pytest.raises(Q.QmoeError):
+            Q.qmoe_encode_dictionary(bad)
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_encode_dictionary(symbols=np.zeros(10, np.int8))      # measured p0 = 1
+
+
+@pytest.fixture(scope="module")
+def words886():
+    return D.build(0.886)
+
+
+@pytest.mark.parametrize("rows,cols,block,p0", [(7, 2080, 256, 0.886), (5, 300, 256, 0.857), (3, 2, 256, 0.886),
+                                               (4, 1030, 64, 0.87), (2, 512, 256, 0.0), (2, 512, 256, 1.0)])
+def test_pack_matches_oracle(words886, rows, cols, block, p0):
+    if p0 in (0.0, 1.0):
+        tern = np.zeros((rows, cols), np.int8) if p0 == 1.0 else \
+            np.where(np.arange(rows * cols).reshape(rows, cols) % 5 < 2, 1, -1).astype(np.int8)
+    else:
+        tern = synth.ternary_matrix(17, 2, 1, rows, cols, p0)
+    codes, off = Q.qmoe_pack(tern, words886, block)
+    rc, ro = C.encode(tern, words886, block)
+    assert np.array_equal(codes, rc) and np.array_equal(off, ro)
+
+
+def test_pack_rejects_bad_input(words886):
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_pack(np.zeros((2, 7), np.int8), words886)
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_pack(np.full((1, 4), 2, np.int8), words886)
+    broken = words886.copy()
+    broken[0] = 0                    # pair count 0 in one half
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_pack(np.zeros((1, 4), np.int8), broken)
+
+
+def test_pack_capacity_error(words886):
+    tern = synth.ternary_matrix(1, 0, 0, 2, 256, 0.886)
+    codes = np.zeros(3, np.uint16)
+    off = np.zeros(3, np.uint32)
+    with pytest.raises(Q.QmoeError) as ei:
+        Q.qmoe_pack_into(tern, words886, 256, codes, off)
+    assert ei.value.status == Q.QMOE_ECAPACITY
+
+
+@pytest.mark.parametrize("p0", [0.886, 0.857])
+def test_compact_table_lists_every_nonzero(p0):
+    ents = D.generate(p0)
+    words = D.pack(ents)
+    comp = Q.qmoe_dict_compact(words)
+    plane_a = comp[:2 * 65536].view(np.uint16)
+    plane_b = comp[2 * 65536:]
+    for e, seq in enumerate(ents):
+        a, b = int(plane_a[e]), int(plane_b[e])
+        assert (a & 15) == len(seq) // 2
+        nz = [2 * i + (1 if s == 1 else 0) for i, s in enumerate(seq) if s]
+        if len(nz) > 3:
+            assert b & 64
+        else:
+            slots = [(a >> 4) & 63, (a >> 10) & 63, b & 63]
+            assert slots == nz + [63] * (3 - len(nz))
+            assert not (b & 64)
+
+
+def test_rvq_pack_matches_oracle():
+    rows, cols = 64, 256
+    w = synth.rvq_weight(4, 1, 2, rows, cols)
+    so, si = synth.rvq_signs(4, 1, 2, rows, cols)
+    wr = R.rotate_weight(w, so, si)
+    u = R.normalised_vectors(wr, R.row_scale_f16(wr), 8)
+    cb = R.fit_codebooks(u, k=256, iters=4, seed=3)
+    cb_bits = cb.astype(np.float16).view(np.uint16)
+    idx, sc = Q.rvq_pack(w, so, si, cb_bits)
+    ridx, rsc = R.encode(wr, cb)
+    assert np.array_equal(sc, rsc)
+    assert np.array_equal(idx, ridx)
+
+
+def test_native_ternary_generator_matches_python():
+    lib = ctypes.CDLL(os.path.join(ROOT, "synth", "libsynth.so"))
+    lib.synth_ternary_rows.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int64,
+                                       ctypes.c_uint32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    for (seed, e, m, cols, p0, r0, n) in [(3, 17, 1, 2080, 0.886, 5, 7), (1, 0, 0, 3072, 0.857, 0, 3)]:
+        out = np.zeros((n, cols), np.int8)
+        lib.synth_ternary_rows(seed, e, m, cols, synth.zero_threshold(p0), r0, n, out.ctypes.data)
+        assert np.array_equal(out, synth.ternary_rows(seed, e, m, cols, p0, r0, n))
