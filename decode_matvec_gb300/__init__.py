@@ -206,7 +206,10 @@ class MatrixSet:
     def from_host(cls, codes: np.ndarray, blk_off: np.ndarray, scale_f16: np.ndarray, rows, cols, block=256,
                   code_base: np.ndarray | None = None, count: int = 1, device="cuda"):
         import torch
-        c = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint16).view(np.int16).copy()).to(device)
+        codes = np.ascontiguousarray(codes, dtype=np.uint16)
+        padded = np.zeros((codes.size + 15) // 8 * 8, dtype=np.uint16)     # whole 16-byte chunks, plus one
+        padded[:codes.size] = codes
+        c = torch.from_numpy(padded.view(np.int16)).to(device)
         o = torch.from_numpy(np.ascontiguousarray(blk_off, dtype=np.uint32).view(np.int32).copy()).to(device)
         s = torch.from_numpy(np.ascontiguousarray(scale_f16, dtype=np.uint16).view(np.int16).copy()).to(device)
         b = None

@@ -36,8 +36,11 @@ constexpr int kDictA = 2 * QMOE_DICT_ENTRIES;          // bytes of the uint16 pl
 constexpr int kDictBytes = QMOE_COMPACT_BYTES;          // both planes
 constexpr int kSlotEmpty = 63;
 constexpr int kSmemMax = 232448;                        // 227 KB opt-in per block
-constexpr int kXsBudgetSmemDict = kSmemMax - kDictBytes - 1024;
-constexpr int kXsBudgetGlobalDict = 48 * 1024;
+constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + row sums, dictionary in SMEM
+constexpr int kBudgetGlobalDict = 56 * 1024;                    // activations + row sums, dictionary via L1/L2
+constexpr int kRowsSmemDict = 128;                              // rows per tile (16 warps x 8 rows)
+constexpr int kThreadsSmemDict = 512;
+constexpr int kThreadsGlobalDict = 256;
 
 struct MatDev {
     const uint16_t* codes;
@@ -73,6 +76,7 @@ struct GemmArgs {
     int nt_max;
     int rows_per_tile;
     int row_tiles;
+    int xs_bytes;                // staged-activation bytes (the row accumulators follow)
     int mode;
     int y_is_f32;
     void* out;
@@ -81,31 +85,24 @@ struct GemmArgs {
 
 __device__ __forceinline__ int nt_class(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
-// Accumulate +-x[p][0..NT) into acc for one compact-table slot.
+// Accumulate +-x[c][0..NT) for one nonzero at staged column c.
 template <int NT>
-__device__ __forceinline__ void apply_slot(int nz, int start, int kcols, float (&acc)[NT],
-                                           const void* xs, bool& bad) {
-    if (nz == kSlotEmpty) return;
-    int p = start + (nz >> 1);
-    if (p >= kcols) {
-        bad = true;
-        return;
-    }
-    float sg = (nz & 1) ? -1.0f : 1.0f;
+__device__ __forceinline__ void add_x(int c, bool neg, float (&acc)[NT], const void* xs) {
+    const float sg = neg ? -1.0f : 1.0f;
     if constexpr (NT == 1) {
-        acc[0] = fmaf(sg, ((const float*)xs)[p], acc[0]);
+        acc[0] = fmaf(sg, ((const float*)xs)[c], acc[0]);
     } else if constexpr (NT == 2) {
-        uint32_t w = ((const uint32_t*)xs)[p];
+        const uint32_t w = ((const uint32_t*)xs)[c];
         acc[0] = fmaf(sg, bf16_lo(w), acc[0]);
         acc[1] = fmaf(sg, bf16_hi(w), acc[1]);
     } else if constexpr (NT == 4) {
-        uint2 w = ((const uint2*)xs)[p];
+        const uint2 w = ((const uint2*)xs)[c];
         acc[0] = fmaf(sg, bf16_lo(w.x), acc[0]);
         acc[1] = fmaf(sg, bf16_hi(w.x), acc[1]);
         acc[2] = fmaf(sg, bf16_lo(w.y), acc[2]);
         acc[3] = fmaf(sg, bf16_hi(w.y), acc[3]);
     } else {
-        uint4 w = ((const uint4*)xs)[p];
+        const uint4 w = ((const uint4*)xs)[c];
         acc[0] = fmaf(sg, bf16_lo(w.x), acc[0]);
         acc[1] = fmaf(sg, bf16_hi(w.x), acc[1]);
         acc[2] = fmaf(sg, bf16_lo(w.y), acc[2]);
@@ -115,6 +112,20 @@ __device__ __forceinline__ void apply_slot(int nz, int start, int kcols, float (
         acc[6] = fmaf(sg, bf16_lo(w.w), acc[6]);
         acc[7] = fmaf(sg, bf16_hi(w.w), acc[7]);
     }
+}
+
+// One compact-table slot (2*position + negative, 63 = empty) of a codeword
+// whose run starts at column `col`.
+template <int NT>
+__device__ __forceinline__ void apply_slot(uint32_t nz, int col, int cols, float (&acc)[NT], const void* xs,
+                                           bool& bad) {
+    if (nz == (uint32_t)kSlotEmpty) return;
+    const int c = col + (int)(nz >> 1);
+    if (c >= cols) {
+        bad = true;
+        return;
+    }
+    add_x<NT>(c, nz & 1u, acc, xs);
 }
 
 template <bool DICT_SMEM>
@@ -129,44 +140,104 @@ __device__ __forceinline__ void lookup(const GemmArgs& a, const uint16_t* sA, co
     }
 }
 
-// One output row of one matrix for NT staged tokens.  Returns the per-token
-// sums (already reduced across the warp) in acc, valid in every lane.
+template <int NT>
+__device__ __forceinline__ void flush_row(float* sacc, int row_local, const float (&acc)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) atomicAdd(sacc + row_local * NT + t, acc[t]);
+}
+
+// A warp streams the codewords of rows [wr0, wr1) of one matrix as one flat
+// sequence, 8 codewords per lane per window (16-byte loads, the next window
+// held in registers while this one is decoded).  Every row expands to exactly
+// `cols` weights, so the running expansion P of a codeword gives its row and
+// column directly: row = wr0 + P / cols, column = P % cols.  Each lane keeps
+// per-token sums for its current row; when its row changes it flushes them to
+// the shared-memory accumulators, and at the end of a window a segmented
+// warp reduction (lanes are ordered by row) lets the first lane of each row
+// segment add that segment's total.  Rows are owned by one warp, but lanes of
+// the warp may flush the same row, so the adds are shared-memory atomics.
 template <int NT, bool DICT_SMEM>
-__device__ __forceinline__ void row_dot(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB,
-                                        const uint16_t* codes, uint32_t n, int cols, const void* xs,
-                                        float (&acc)[NT], int lane) {
+__device__ void stream_rows(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const uint16_t* codes,
+                            uint64_t g_lo, uint64_t g_hi, int cols, int n_rows, const void* xs, float* sacc,
+                            int lane) {
+    bool bad = false;
+    float acc[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-    int pos = 0;
-    bool bad = false;
-    uint32_t code_next = lane < n ? (uint32_t)__ldg(codes + lane) : 0u;
-    for (uint32_t i = 0; i < n; i += 32) {
-        const uint32_t code = code_next;
-        const bool valid = i + lane < n;
-        if (i + 32 + lane < n) code_next = (uint32_t)__ldg(codes + i + 32 + lane);
-        // lanes past the end of the row: run length 0 and all three slots empty
-        uint32_t ea = (kSlotEmpty << 4) | (kSlotEmpty << 10), eb = kSlotEmpty;
-        if (valid) lookup<DICT_SMEM>(a, sA, sB, code, ea, eb);
-        const int len = (int)(ea & 15u) * 2;
-        const int incl = warp_incl_scan(len, lane);
-        const int start = pos + incl - len;
-        apply_slot<NT>((int)((ea >> 4) & 63u), start, cols, acc, xs, bad);
-        apply_slot<NT>((int)(ea >> 10), start, cols, acc, xs, bad);
-        apply_slot<NT>((int)(eb & 63u), start, cols, acc, xs, bad);
-        if (eb & 64u) {
-            // entry with more than three nonzeros: walk its canonical words
-            const uint32_t w0 = __ldg(a.words + 2 * code), w1 = __ldg(a.words + 2 * code + 1);
-            for (int q = 0; q < len; ++q) {
-                const uint32_t s = ((q < 14 ? w0 : w1) >> (4 + 2 * (q % 14))) & 3u;
-                if (s == 1u || s == 2u) apply_slot<NT>(2 * q + (s == 1u ? 1 : 0), start, cols, acc, xs, bad);
+    uint32_t P = 0;                               // weights expanded before this window
+    const uint64_t w0 = g_lo & ~7ull;
+    uint4 nxt = make_uint4(0, 0, 0, 0);
+    if (w0 + 8 * lane < g_hi) nxt = __ldg((const uint4*)(codes + w0 + 8 * lane));
+    for (uint64_t w = w0; w < g_hi; w += 256) {
+        const uint64_t my = w + 8 * (uint64_t)lane;
+        const uint4 cur = nxt;
+        if (my + 256 < g_hi) nxt = __ldg((const uint4*)(codes + my + 256));
+        const uint32_t cw[4] = {cur.x, cur.y, cur.z, cur.w};
+        uint32_t ea[8], eb[8];
+        int sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+            const bool valid = my + j >= g_lo && my + j < g_hi;
+            ea[j] = (kSlotEmpty << 4) | (kSlotEmpty << 10);
+            eb[j] = kSlotEmpty;
+            if (valid) lookup<DICT_SMEM>(a, sA, sB, code, ea[j], eb[j]);
+            sum += (int)(ea[j] & 15u) * 2;
+        }
+        const int incl = warp_incl_scan(sum, lane);
+        const uint32_t start = P + (uint32_t)(incl - sum);
+        int row = (int)(start / (uint32_t)cols);
+        int col = (int)(start - (uint32_t)row * (uint32_t)cols);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int len = (int)(ea[j] & 15u) * 2;
+            if (len == 0) continue;
+            if (row >= n_rows) {
+                bad = true;
+                continue;
+            }
+            apply_slot<NT>((ea[j] >> 4) & 63u, col, cols, acc, xs, bad);
+            apply_slot<NT>(ea[j] >> 10, col, cols, acc, xs, bad);
+            apply_slot<NT>(eb[j] & 63u, col, cols, acc, xs, bad);
+            if (eb[j] & 64u) {
+                // more than three nonzeros: walk the canonical entry
+                const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+                const uint32_t c0 = __ldg(a.words + 2 * code), c1 = __ldg(a.words + 2 * code + 1);
+                for (int q = 0; q < len; ++q) {
+                    const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
+                    if (s == 1u || s == 2u) apply_slot<NT>(2u * q + (s == 1u ? 1u : 0u), col, cols, acc, xs, bad);
+                }
+            }
+            col += len;
+            if (col >= cols) {
+                // the run ended this row (codewords never cross a row)
+                if (col > cols) bad = true;
+                flush_row<NT>(sacc, row, acc);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+                col = 0;
+                ++row;
             }
         }
-        pos += __shfl_sync(QMOE_FULL_MASK, incl, 31);
-    }
-    if (lane == 0 && (pos != cols)) bad = true;
-    if (__any_sync(QMOE_FULL_MASK, bad) && lane == 0) set_error(QMOE_EFORMAT);
+        // segmented reduction of the lanes' open rows (lanes are in row order)
+        const int r_clamped = min(row, n_rows - 1);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = warp_sum(acc[t]);
+        for (int d = 1; d < 32; d <<= 1) {
+            const int r_from = __shfl_down_sync(QMOE_FULL_MASK, r_clamped, d);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const float v = __shfl_down_sync(QMOE_FULL_MASK, acc[t], d);
+                if (lane + d < 32 && r_from == r_clamped) acc[t] += v;
+            }
+        }
+        const int r_prev = __shfl_up_sync(QMOE_FULL_MASK, r_clamped, 1);
+        if ((lane == 0 || r_prev != r_clamped) && row < n_rows) flush_row<NT>(sacc, r_clamped, acc);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+        P += (uint32_t)__shfl_sync(QMOE_FULL_MASK, incl, 31);
+    }
+    if (lane == 0 && P != (uint32_t)n_rows * (uint32_t)cols) bad = true;
+    if (__any_sync(QMOE_FULL_MASK, bad) && lane == 0) set_error(QMOE_EFORMAT);
 }
 
 __device__ __forceinline__ void job_of(const GemmArgs& a, int j, Job& job) {
@@ -203,55 +274,90 @@ __device__ void stage_x(const GemmArgs& a, const Job& job, void* xs, int tid, in
     }
 }
 
+// Scale, activation and store of the tile's rows (threads over rows, per token).
 template <int NT>
-__device__ __forceinline__ void epilogue(const GemmArgs& a, const Job& job, int row, float s,
-                                         const float (&acc)[NT], int lane) {
+__device__ void tile_epilogue(const GemmArgs& a, const Job& job, int r0, int nr, const float* sacc, int tid,
+                              int nthreads) {
     const int rows = a.m.rows;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        if (lane == t && t < job.n_tok) {
-            const int slot = slot_at(a, job, t);
-            const float v = s * acc[t];
-            switch (a.mode) {
-                case OUT_PLAIN:
-                    if (a.y_is_f32) ((float*)a.out)[(size_t)slot * rows + row] = v;
-                    else ((uint16_t*)a.out)[(size_t)slot * rows + row] = f32_to_bf16(v);
-                    break;
-                case OUT_RELU_H:
-                    ((uint16_t*)a.out)[(size_t)slot * rows + row] = f32_to_bf16(fmaxf(v, 0.0f));
-                    break;
-                case OUT_GATED: {
-                    const float g = a.gates[slot] * v;
-                    if (a.y_is_f32) ((float*)a.out)[(size_t)slot * rows + row] = g;
-                    else ((uint16_t*)a.out)[(size_t)slot * rows + row] = f32_to_bf16(g);
-                    break;
-                }
-                default:
-                    ((float*)a.out)[(size_t)slot * rows + row] = v;
-                    break;
+    const uint16_t* scale = a.m.scale + (size_t)job.matrix * rows;
+    for (int i = tid; i < nr * job.n_tok; i += nthreads) {
+        const int t = i / nr, rl = i - t * nr, row = r0 + rl;
+        const int slot = slot_at(a, job, t);
+        const float v = f16_to_f32(scale[row]) * sacc[rl * NT + t];
+        const size_t o = (size_t)slot * rows + row;
+        switch (a.mode) {
+            case OUT_PLAIN:
+                if (a.y_is_f32) ((float*)a.out)[o] = v;
+                else ((uint16_t*)a.out)[o] = f32_to_bf16(v);
+                break;
+            case OUT_RELU_H:
+                ((uint16_t*)a.out)[o] = f32_to_bf16(fmaxf(v, 0.0f));
+                break;
+            case OUT_GATED: {
+                const float g = a.gates[slot] * v;
+                if (a.y_is_f32) ((float*)a.out)[o] = g;
+                else ((uint16_t*)a.out)[o] = f32_to_bf16(g);
+                break;
             }
+            default:
+                ((float*)a.out)[o] = v;
+                break;
         }
     }
 }
 
-template <int NT, bool DICT_SMEM>
-__device__ void tile_rows(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const Job& job,
-                          int r0, const void* xs, int warp, int nwarps, int lane) {
+__device__ __forceinline__ void tile_rows_of(const GemmArgs& a, int tile, Job& job, int& r0, int& r1) {
+    job_of(a, tile / a.row_tiles, job);
+    r0 = (tile % a.row_tiles) * a.rows_per_tile;
+    r1 = min(a.m.rows, r0 + a.rows_per_tile);
+}
+
+// Warms L2 with the code range of a tile this block will process next.
+__device__ void prefetch_tile(const GemmArgs& a, int tile, int n_tiles) {
+    if (tile >= n_tiles) return;
+    Job job;
+    int r0, r1;
+    tile_rows_of(a, tile, job, r0, r1);
     const MatDev& m = a.m;
     const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
-    const uint16_t* codes = m.codes + (m.code_base ? m.code_base[job.matrix] : 0ull);
-    const uint16_t* scale = m.scale + (size_t)job.matrix * m.rows;
-    const int r1 = min(m.rows, r0 + a.rows_per_tile);
-    for (int r = r0 + warp; r < r1; r += nwarps) {
-        const uint32_t lo = off[(size_t)r * m.nb], hi = off[(size_t)(r + 1) * m.nb];
+    const uint64_t base = m.code_base ? m.code_base[job.matrix] : 0ull;
+    const uint64_t lo = (base + off[(size_t)r0 * m.nb]) & ~7ull;
+    const uint64_t hi = (base + off[(size_t)r1 * m.nb] + 7) & ~7ull;
+    if (hi <= lo) return;
+    const char* p = (const char*)(m.codes + lo);
+    uint64_t bytes = (hi - lo) * 2;
+    while (bytes) {
+        const uint32_t n = (uint32_t)(bytes < (1ull << 20) ? bytes : (1ull << 20));
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+        p += n;
+        bytes -= n;
+    }
+}
+
+template <int NT, bool DICT_SMEM>
+__device__ void run_tile(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const Job& job, int r0, int r1,
+                         void* xs, float* sacc, int tid, int nthreads, int warp, int nwarps, int lane) {
+    const MatDev& m = a.m;
+    stage_x<NT>(a, job, xs, tid, nthreads);
+    const int nr = r1 - r0;
+    for (int i = tid; i < nr * NT; i += nthreads) sacc[i] = 0.0f;
+    __syncthreads();
+    const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
+    const uint64_t base = m.code_base ? m.code_base[job.matrix] : 0ull;
+    const int per = (nr + nwarps - 1) / nwarps;
+    const int wr0 = r0 + warp * per, wr1 = min(r1, wr0 + per);
+    if (wr0 < wr1) {
+        const uint32_t lo = off[(size_t)wr0 * m.nb], hi = off[(size_t)wr1 * m.nb];
         if (hi < lo) {
             if (lane == 0) set_error(QMOE_EFORMAT);
-            continue;
+        } else {
+            stream_rows<NT, DICT_SMEM>(a, sA, sB, m.codes, base + lo, base + hi, m.cols, wr1 - wr0, xs,
+                                       sacc + (wr0 - r0) * NT, lane);
         }
-        float acc[NT];
-        row_dot<NT, DICT_SMEM>(a, sA, sB, codes + lo, hi - lo, m.cols, xs, acc, lane);
-        epilogue<NT>(a, job, r, f16_to_f32(scale[r]), acc, lane);
     }
+    __syncthreads();
+    tile_epilogue<NT>(a, job, r0, nr, sacc, tid, nthreads);
+    __syncthreads();
 }
 
 template <bool DICT_SMEM>
@@ -262,6 +368,12 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
     const uint16_t* sA = nullptr;
     const uint8_t* sB = nullptr;
     unsigned char* xs = smem;
+    const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
+    const int n_tiles = n_jobs * a.row_tiles;
+    if (tid == 0) {
+        prefetch_tile(a, blockIdx.x, n_tiles);
+        prefetch_tile(a, blockIdx.x + gridDim.x, n_tiles);
+    }
     if constexpr (DICT_SMEM) {
         const uint4* srcA = (const uint4*)a.dictA;
         const uint4* srcB = (const uint4*)a.dictB;
@@ -271,29 +383,20 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
         sA = (const uint16_t*)smem;
         sB = (const uint8_t*)(smem + kDictA);
         xs = smem + kDictBytes;
-        __syncthreads();
     }
-    const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
-    const int n_tiles = n_jobs * a.row_tiles;
+    float* sacc = (float*)(xs + a.xs_bytes);
+    __syncthreads();
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        if (tid == 0) prefetch_tile(a, tile + 2 * gridDim.x, n_tiles);
         Job job;
-        job_of(a, tile / a.row_tiles, job);
-        const int r0 = (tile % a.row_tiles) * a.rows_per_tile;
-        const int nt = nt_class(job.n_tok);
-        switch (nt) {
-            case 1: stage_x<1>(a, job, xs, tid, nthreads); break;
-            case 2: stage_x<2>(a, job, xs, tid, nthreads); break;
-            case 4: stage_x<4>(a, job, xs, tid, nthreads); break;
-            default: stage_x<8>(a, job, xs, tid, nthreads); break;
+        int r0, r1;
+        tile_rows_of(a, tile, job, r0, r1);
+        switch (nt_class(job.n_tok)) {
+            case 1: run_tile<1, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
+            case 2: run_tile<2, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
+            case 4: run_tile<4, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
+            default: run_tile<8, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
         }
-        __syncthreads();
-        switch (nt) {
-            case 1: tile_rows<1, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
-            case 2: tile_rows<2, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
-            case 4: tile_rows<4, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
-            default: tile_rows<8, DICT_SMEM>(a, sA, sB, job, r0, xs, warp, nwarps, lane); break;
-        }
-        __syncthreads();
     }
 }
 
@@ -513,13 +616,24 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
 // ------------------------------------------------------------ host side
 int g_sm_count[64];
 
-int nt_max_for(int cols, int budget) {
-    for (int nt = 8; nt >= 2; nt >>= 1)
-        if (cols * nt * 2 <= budget) return nt;
-    return cols * 4 <= budget ? 1 : 0;
+size_t xs_bytes(int cols, int nt) { return ((nt == 1 ? (size_t)cols * 4 : (size_t)cols * nt * 2) + 15) & ~(size_t)15; }
+
+size_t tile_smem(int cols, int nt, int rows_per_tile) { return xs_bytes(cols, nt) + (size_t)rows_per_tile * nt * 4; }
+
+// Largest token chunk (8, 4, 2, 1) whose staged activations and row sums fit the budget.
+int nt_max_for(int cols, int budget, int rows_per_tile) {
+    for (int nt = 8; nt >= 1; nt >>= 1)
+        if (tile_smem(cols, nt, rows_per_tile) <= (size_t)budget) return nt;
+    return 0;
 }
 
-size_t xs_bytes(int cols, int nt_max) { return nt_max == 1 ? (size_t)cols * 4 : (size_t)cols * nt_max * 2; }
+// Rows per tile of the L1/L2-dictionary variant: enough tiles to fill the GPU.
+int rows_per_tile_small(int rows, long long n_jobs) {
+    const long long want = 2LL * qmoe::sm_count();
+    long long rpt = (long long)rows * std::max(1LL, n_jobs) / want;
+    rpt = std::max(8LL, std::min(64LL, rpt / 8 * 8));
+    return (int)rpt;
+}
 
 bool valid_set(const qmoe_matrix_set* s) {
     return s && s->codes && s->blk_off && s->scale_f16 && s->count >= 1 && s->rows >= 1 && s->cols >= 2 &&
@@ -540,27 +654,27 @@ MatDev to_dev(const qmoe_matrix_set* s) {
     return m;
 }
 
-int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, cudaStream_t st, int grid_hint) {
+int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaStream_t st, long long tiles_hint) {
     const int sms = qmoe::sm_count();
+    a.nt_max = nt_max;
+    a.rows_per_tile = rows_per_tile;
+    a.row_tiles = (a.m.rows + rows_per_tile - 1) / rows_per_tile;
+    a.xs_bytes = (int)xs_bytes(a.m.cols, nt_max);
+    const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + tile_smem(a.m.cols, nt_max, rows_per_tile);
+    if (smem > (size_t)kSmemMax) return qmoe::fail(QMOE_EUNSUPPORTED, "dict_gemm: tile does not fit in shared memory");
     if (dict_smem) {
-        const size_t smem = kDictBytes + xs_bytes(a.m.cols, nt_max);
         int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<true>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
                                   "cudaFuncSetAttribute");
         if (rc) return rc;
-        a.rows_per_tile = 128;
-        a.row_tiles = (a.m.rows + 127) / 128;
-        dict_gemm_kernel<true><<<sms, 512, smem, st>>>(a);
+        dict_gemm_kernel<true><<<sms, kThreadsSmemDict, smem, st>>>(a);
     } else {
-        const size_t smem = xs_bytes(a.m.cols, nt_max);
         int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<false>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
                                   "cudaFuncSetAttribute");
         if (rc) return rc;
-        a.rows_per_tile = 8;
-        a.row_tiles = (a.m.rows + 7) / 8;
-        int grid = grid_hint > 0 ? std::min(grid_hint, sms * 8) : sms * 4;
-        dict_gemm_kernel<false><<<std::max(grid, 1), 256, smem, st>>>(a);
+        const long long grid = std::max(1LL, std::min(tiles_hint, (long long)sms * 4));
+        dict_gemm_kernel<false><<<(unsigned)grid, kThreadsGlobalDict, smem, st>>>(a);
     }
     return qmoe::launch_check("dict_gemm_kernel");
 }
@@ -625,7 +739,7 @@ extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* 
     if (T < 0) return fail(QMOE_EINVAL, "qmoe_expert_matvec: T < 0");
     if (T == 0) return QMOE_OK;
     if (!x_bf16 || !y) return fail(QMOE_EINVAL, "qmoe_expert_matvec: NULL x or y");
-    const int nt_max = nt_max_for(mat->cols, kXsBudgetGlobalDict);
+    const int nt_max = nt_max_for(mat->cols, kBudgetGlobalDict, 64);
     if (!nt_max) return fail(QMOE_EUNSUPPORTED, "qmoe_expert_matvec: cols too large");
     GemmArgs a{};
     a.dictA = (const uint16_t*)dict->compact;
@@ -637,13 +751,12 @@ extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* 
     a.jobs = nullptr;
     a.slots = nullptr;
     a.T_implicit = T;
-    a.nt_max = nt_max;
     a.mode = OUT_PLAIN;
     a.y_is_f32 = y_is_f32 ? 1 : 0;
     a.out = y;
-    const int jobs = (T + nt_max - 1) / nt_max;
-    const int tiles = jobs * ((mat->rows + 7) / 8);
-    return launch_gemm(a, false, nt_max, (cudaStream_t)stream, tiles);
+    const long long jobs = (T + nt_max - 1) / nt_max;
+    const int rpt = rows_per_tile_small(mat->rows, jobs);
+    return launch_gemm(a, false, nt_max, rpt, (cudaStream_t)stream, jobs * ((mat->rows + rpt - 1) / rpt));
 }
 
 extern "C" int qmoe_route(const float* logits, int T, int E, int k, int32_t* ids, float* gates, void* stream) {
@@ -728,8 +841,10 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     if (ws_bytes < w.bytes) return fail(QMOE_ECAPACITY, "qmoe_moe_layer: workspace too small");
     const long long slots = (long long)T * k;
     const bool big = slots >= 16;
-    const int budget = big ? kXsBudgetSmemDict : kXsBudgetGlobalDict;
-    const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
+    const int budget = big ? kBudgetSmemDict : kBudgetGlobalDict;
+    const int rpt_wi = big ? kRowsSmemDict : rows_per_tile_small(d_ff, slots);
+    const int rpt_wo = big ? kRowsSmemDict : rows_per_tile_small(d_model, slots);
+    const int nt_wi = nt_max_for(d_model, budget, rpt_wi), nt_wo = nt_max_for(d_ff, budget, rpt_wo);
     if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
     cudaStream_t st = (cudaStream_t)stream;
     qmoe::phase_event(0, st);
@@ -751,10 +866,9 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     a.x_div = k;
     a.jobs = w.jobs_a;
     a.n_jobs_dev = w.n_jobs;
-    a.nt_max = nt_wi;
     a.mode = OUT_RELU_H;
     a.out = w.h;
-    rc = launch_gemm(a, big, nt_wi, st, (int)std::min<long long>(slots * ((d_ff + 7) / 8), 1 << 20));
+    rc = launch_gemm(a, big, nt_wi, rpt_wi, st, slots * ((d_ff + rpt_wi - 1) / rpt_wi));
     if (rc) return rc;
     qmoe::phase_event(2, st);
     // wo: o[slot] = Wo h[slot]; gated straight into y when k == 1
@@ -763,10 +877,9 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     a.x_div = 1;
     a.jobs = w.jobs_b;
     a.n_jobs_dev = w.n_jobs + 1;
-    a.nt_max = nt_wo;
     a.mode = k == 1 ? OUT_GATED : OUT_SLOT_F32;
     a.out = k == 1 ? y : (void*)w.o;
-    rc = launch_gemm(a, big, nt_wo, st, (int)std::min<long long>(slots * ((d_model + 7) / 8), 1 << 20));
+    rc = launch_gemm(a, big, nt_wo, rpt_wo, st, slots * ((d_model + rpt_wo - 1) / rpt_wo));
     if (rc) return rc;
     qmoe::phase_event(3, st);
     if (k > 1) {

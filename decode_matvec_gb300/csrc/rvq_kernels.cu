@@ -269,6 +269,252 @@ __global__ void __launch_bounds__(kRvqThreads) rvq_gemm_kernel(const RvqGemmArgs
     }
 }
 
+// ---------------------------------------------------------------- decode-multiply (tcgen05 tensor cores)
+// For T >= 16 the RVQ product is a real dense contraction per expert: a CTA
+// takes 128 output rows of one expert matrix and up to 32 of its tokens.  For
+// every 128-wide K chunk, 256 threads decode the 128 x 128 weight tile
+// (C1[i1] + C2[i2] in fp32, rounded to fp16) and the 32 x 128 activation tile
+// (fp32 -> fp16) into shared memory in the canonical no-swizzle K-major layout
+// (8-row x 16-byte core matrices; neighbours along K 128 B apart, along M/N
+// 2048 B apart); one thread issues eight tcgen05.mma (M=128, N=32, K=16,
+// fp16 x fp16 -> fp32 in tensor memory) and commits them to the buffer's
+// mbarrier, while the threads decode the next chunk into the other buffer.
+// The row scale is applied in the epilogue (tcgen05.ld of the accumulator).
+// Every mbarrier wait is bounded: on expiry the kernel records QMOE_ETIMEOUT,
+// still frees its tensor memory and returns.
+
+constexpr int kTcM = 128, kTcN = 32, kTcK = 128;
+constexpr int kTcThreads = 256;
+constexpr int kTcLBO = 128;                       // core matrices adjacent along K
+constexpr int kTcSBO = (kTcK / 8) * 128;          // core matrices adjacent along M / N (2048 B)
+constexpr int kTcABytes = kTcM * kTcK * 2;        // 32 KB
+constexpr int kTcBBytes = kTcN * kTcK * 2;        // 8 KB
+constexpr int kTcSmem = 1024 /*align*/ + 2 * 256 * 16 /*codebooks*/ + 2 * (kTcABytes + kTcBBytes) + 64;
+constexpr uint32_t kTcSpinLimit = 1u << 20;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(kTcLBO >> 4) << 16;
+    d |= (uint64_t)(kTcSBO >> 4) << 32;
+    d |= 1ull << 46;                              // descriptor version for tcgen05
+    return d;                                     // base offset 0, swizzle none
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N = 32, M = 128.
+constexpr uint32_t kTcIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
+                              ((uint32_t)(kTcM >> 4) << 24);
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kTcSpinLimit; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void store_half8(uint8_t* dst, const float (&v)[8]) {
+    __half2 h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+    *(uint4*)dst = *(const uint4*)h;
+}
+
+__global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint4* scb = (uint4*)smem;
+    uint8_t* abuf = smem + 2 * 256 * 16;                         // 2 x 32 KB
+    uint8_t* bbuf = abuf + 2 * kTcABytes;                         // 2 x 8 KB
+    uint64_t* bars = (uint64_t*)(bbuf + 2 * kTcBBytes);           // 2 mbarriers
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const RvqDev& m = a.m;
+
+    for (int i = tid; i < 2 * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)m.cb + i);
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + b)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTcN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    uint32_t commits[2] = {0, 0};     // commits issued per buffer (tracked identically by every thread)
+    uint32_t waited[2] = {0, 0};
+    bool timed_out = false;
+    const int nv = m.cols / 8;
+    const int nk = m.cols / kTcK;
+    const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + kTcN - 1) / kTcN;
+    const int n_tiles = n_jobs * a.row_tiles;
+
+    for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+        Job job;
+        const int j = tile / a.row_tiles;
+        if (a.jobs) {
+            job = a.jobs[j];
+        } else {
+            job.matrix = 0;
+            job.slot_begin = j * kTcN;
+            job.n_tok = min(kTcN, a.T_implicit - j * kTcN);
+        }
+        const int r0 = (tile % a.row_tiles) * kTcM;
+        for (int kc = 0; kc < nk; ++kc) {
+            const int b = kc & 1;
+            if (commits[b] > waited[b]) {
+                // the MMAs that last read this buffer must be done before it is rewritten
+                if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
+                ++waited[b];
+            }
+            uint8_t* A = abuf + b * kTcABytes;
+            uint8_t* B = bbuf + b * kTcBBytes;
+            // A: thread -> (row, half of the chunk's 16 vectors)
+            {
+                const int rl = tid >> 1, half = tid & 1;
+                const int row = r0 + rl;
+                float w[8];
+                uint4 pairs = make_uint4(0, 0, 0, 0);
+                if (row < m.rows) {
+                    const uint8_t* ip = m.idx + (((size_t)job.matrix * m.rows + row) * nv + kc * (kTcK / 8) + half * 8) * 2;
+                    pairs = __ldg((const uint4*)ip);
+                }
+                const uint32_t pw[4] = {pairs.x, pairs.y, pairs.z, pairs.w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t pr = (pw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+                    if (row < m.rows) {
+                        decode8(scb[pr & 255u], scb[256 + (pr >> 8)], w);
+                    } else {
+#pragma unroll
+                        for (int z = 0; z < 8; ++z) w[z] = 0.0f;
+                    }
+                    const int c8 = half * 8 + q;
+                    store_half8(A + (rl >> 3) * kTcSBO + c8 * kTcLBO + (rl & 7) * 16, w);
+                }
+            }
+            // B: thread -> (token, two 8-wide K groups)
+            {
+                const int n = tid >> 3, g = tid & 7;
+                float v[8];
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c8 = g * 2 + h2;
+                    if (n < job.n_tok) {
+                        const int slot = a.slots ? a.slots[job.slot_begin + n] : job.slot_begin + n;
+                        const float4* src = (const float4*)(a.xr + (size_t)slot * m.cols + kc * kTcK + c8 * 8);
+                        const float4 p0 = src[0], p1 = src[1];
+                        v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+                        v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+                    } else {
+#pragma unroll
+                        for (int z = 0; z < 8; ++z) v[z] = 0.0f;
+                    }
+                    store_half8(B + (n >> 3) * kTcSBO + c8 * kTcLBO + (n & 7) * 16, v);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (__syncthreads_or(timed_out)) {
+                timed_out = true;
+                break;
+            }
+            if (tid == 0) {
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+#pragma unroll
+                for (int k = 0; k < kTcK / 16; ++k) {
+                    const uint64_t ad = umma_desc(a0 + k * 2 * kTcLBO);
+                    const uint64_t bd = umma_desc(b0 + k * 2 * kTcLBO);
+                    const uint32_t accum = (kc > 0 || k > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+                        "l"(ad), "l"(bd), "r"(kTcIdesc), "r"(accum)
+                        : "memory");
+                }
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 smem_u32(bars + b))
+                             : "memory");
+            }
+            ++commits[b];
+        }
+        // wait for every outstanding commit, oldest first
+        for (int q = 0; q < 2; ++q) {
+            const int b = (nk + q) & 1;   // the buffer whose commit is older comes first
+            while (commits[b] > waited[b]) {
+                if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
+                ++waited[b];
+            }
+        }
+        timed_out = __syncthreads_or(timed_out);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (warp < 4 && !timed_out) {
+            uint32_t r[32];
+            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                  "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                  "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                  "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                : "r"(taddr));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            const int row = r0 + 32 * warp + lane;
+            if (row < m.rows) {
+                const float s = f16_to_f32(m.scale[(size_t)job.matrix * m.rows + row]);
+#pragma unroll
+                for (int n = 0; n < kTcN; ++n) {
+                    if (n < job.n_tok) {
+                        const int slot = a.slots ? a.slots[job.slot_begin + n] : job.slot_begin + n;
+                        a.out[(size_t)slot * m.rows + row] = s * __uint_as_float(r[n]);
+                    }
+                }
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+    }
+    if (timed_out) {
+        // give the tensor core one more bounded chance to finish before the memory is freed
+        for (int b = 0; b < 2; ++b)
+            while (commits[b] > waited[b]) {
+                mbar_wait(smem_u32(bars + b), waited[b] & 1u);
+                ++waited[b];
+            }
+        if (tid == 0) atomicCAS(&g_rvq_error, 0, QMOE_ETIMEOUT);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcN) : "memory");
+}
+
+int launch_rvq_tc(RvqGemmArgs a, cudaStream_t st, long long tiles_hint) {
+    int rc = qmoe::cuda_check(
+        cudaFuncSetAttribute(rvq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem), "rvq tc attr");
+    if (rc) return rc;
+    a.rows_per_tile = kTcM;
+    a.row_tiles = (a.m.rows + kTcM - 1) / kTcM;
+    const long long grid = std::max(1LL, std::min(tiles_hint, (long long)qmoe::sm_count() * 2));
+    rvq_tc_kernel<<<(unsigned)grid, kTcThreads, kTcSmem, st>>>(a);
+    return qmoe::launch_check("rvq_tc_kernel");
+}
+
 // ---------------------------------------------------------------- decode (test)
 __global__ void rvq_decode_kernel(RvqDev m, float* __restrict__ out) {
     const size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
@@ -304,6 +550,9 @@ int nt_for(int cols) {
     // staged activations: cols * nt * 4 bytes, at most 64 KB
     return cols * 8 * 4 <= 65536 ? 8 : cols * 4 * 4 <= 65536 ? 4 : 1;
 }
+
+// Tensor-core path: batches of 16+ activation rows and K a multiple of the 128-wide chunk.
+bool use_tc(long long rows_of_x, int cols) { return rows_of_x >= 16 && cols % kTcK == 0; }
 
 float inv_sqrt(int n) { return (float)(1.0 / std::sqrt((double)n)); }
 
@@ -364,7 +613,8 @@ extern "C" int rvq_expert_matmul(const rvq_matrix_set* mat, const void* x_bf16, 
     a.T_implicit = T;
     a.nt_max = nt_for(cols);
     a.out = yr;
-    rc = launch_rvq_gemm(a, st);
+    if (use_tc(T, cols)) rc = launch_rvq_tc(a, st, (long long)((T + kTcN - 1) / kTcN) * ((rows + kTcM - 1) / kTcM));
+    else rc = launch_rvq_gemm(a, st);
     if (rc) return rc;
     out_transform_kernel<<<T, fwht_threads(rows), 2 * rows * sizeof(float), st>>>(
         yr, nullptr, mat->sign_out, nullptr, 1, rows, inv_sqrt(rows), y, y_is_f32 ? 1 : 0);
@@ -440,7 +690,11 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     if (ws_bytes < w.bytes) return fail(QMOE_ECAPACITY, "rvq_moe_layer: workspace too small");
     cudaStream_t st = (cudaStream_t)stream;
     const int slots = T * k;
-    const int nt_a = nt_for(d_model), nt_b = nt_for(d_ff);
+    const bool tc = use_tc(slots, d_model) && use_tc(slots, d_ff);
+    const int nt_a = tc ? kTcN : nt_for(d_model), nt_b = tc ? kTcN : nt_for(d_ff);
+    auto gemm = [&](RvqGemmArgs& ga, int rows) {
+        return tc ? launch_rvq_tc(ga, st, (long long)slots * ((rows + kTcM - 1) / kTcM)) : launch_rvq_gemm(ga, st);
+    };
     qmoe::phase_event(0, st);
     int rc = qmoe::launch_plan(ids, slots, E, nt_a, nt_b, w.counts, w.offsets, w.perm, w.jobs_a, w.jobs_b, w.n_jobs, st);
     if (rc) return rc;
@@ -457,11 +711,11 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     a.m = to_dev(gate);
     a.xr = w.xg;
     a.out = w.gp;
-    if ((rc = launch_rvq_gemm(a, st))) return rc;
+    if ((rc = gemm(a, d_ff))) return rc;
     a.m = to_dev(up);
     a.xr = w.xu;
     a.out = w.up;
-    if ((rc = launch_rvq_gemm(a, st))) return rc;
+    if ((rc = gemm(a, d_ff))) return rc;
     qmoe::phase_event(2, st);
     swiglu_transform_kernel<<<slots, fwht_threads(d_ff), 2 * d_ff * sizeof(float), st>>>(
         w.gp, w.up, ids, gate->sign_out, up->sign_out, down->sign_in, d_ff, inv_sqrt(d_ff), w.hr);
@@ -473,7 +727,7 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     a.m = to_dev(down);
     a.xr = w.hr;
     a.out = w.dp;
-    if ((rc = launch_rvq_gemm(a, st))) return rc;
+    if ((rc = gemm(a, d_model))) return rc;
     qmoe::phase_event(4, st);
     out_transform_kernel<<<T, fwht_threads(d_model), 2 * d_model * sizeof(float), st>>>(
         w.dp, ids, down->sign_out, gates, k, d_model, inv_sqrt(d_model), y, y_is_f32 ? 1 : 0);

@@ -145,6 +145,12 @@ typedef struct {
  * codes[code_base[e]]; its block offsets are blk_off[e*(rows*nb+1) + ...],
  * relative to code_base[e], nb = ceil(cols/block); its scales are
  * scale_f16[e*rows + r].  code_base may be NULL when count == 1 (base 0).
+ * The kernels read codewords in aligned 16-byte chunks: `codes` must be
+ * 16-byte aligned and its allocation must extend (zero-padded) to the next
+ * multiple of 8 codewords after the last codeword of the set.  Offsets must
+ * lie inside the codes allocation; the kernels check that each row expands to
+ * exactly `cols` weights (QMOE_EFORMAT otherwise) but cannot check offsets
+ * against the allocation size.
  */
 typedef struct {
     const uint16_t* codes;      /* device */
