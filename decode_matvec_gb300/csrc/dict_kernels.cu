@@ -38,7 +38,7 @@ constexpr int kSlotEmpty = 63;
 constexpr int kSmemMax = 232448;                        // 227 KB opt-in per block
 constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + row sums, dictionary in SMEM
 constexpr int kBudgetGlobalDict = 56 * 1024;                    // activations + row sums, dictionary via L1/L2
-constexpr int kRowsSmemDict = 128;                              // rows per tile (16 warps x 8 rows)
+constexpr int kSaccBytes = 4096;                                // per-tile row sums (rows x tokens x 4 B)
 constexpr int kThreadsSmemDict = 512;
 constexpr int kThreadsGlobalDict = 256;
 
@@ -77,6 +77,7 @@ struct GemmArgs {
     int rows_per_tile;
     int row_tiles;
     int xs_bytes;                // staged-activation bytes (the row accumulators follow)
+    float inv_cols;              // 1 / cols, for row = P / cols
     int mode;
     int y_is_f32;
     void* out;
@@ -85,47 +86,31 @@ struct GemmArgs {
 
 __device__ __forceinline__ int nt_class(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
-// Accumulate +-x[c][0..NT) for one nonzero at staged column c.
-template <int NT>
-__device__ __forceinline__ void add_x(int c, bool neg, float (&acc)[NT], const void* xs) {
-    const float sg = neg ? -1.0f : 1.0f;
-    if constexpr (NT == 1) {
-        acc[0] = fmaf(sg, ((const float*)xs)[c], acc[0]);
-    } else if constexpr (NT == 2) {
-        const uint32_t w = ((const uint32_t*)xs)[c];
-        acc[0] = fmaf(sg, bf16_lo(w), acc[0]);
-        acc[1] = fmaf(sg, bf16_hi(w), acc[1]);
-    } else if constexpr (NT == 4) {
-        const uint2 w = ((const uint2*)xs)[c];
-        acc[0] = fmaf(sg, bf16_lo(w.x), acc[0]);
-        acc[1] = fmaf(sg, bf16_hi(w.x), acc[1]);
-        acc[2] = fmaf(sg, bf16_lo(w.y), acc[2]);
-        acc[3] = fmaf(sg, bf16_hi(w.y), acc[3]);
-    } else {
-        const uint4 w = ((const uint4*)xs)[c];
-        acc[0] = fmaf(sg, bf16_lo(w.x), acc[0]);
-        acc[1] = fmaf(sg, bf16_hi(w.x), acc[1]);
-        acc[2] = fmaf(sg, bf16_lo(w.y), acc[2]);
-        acc[3] = fmaf(sg, bf16_hi(w.y), acc[3]);
-        acc[4] = fmaf(sg, bf16_lo(w.z), acc[4]);
-        acc[5] = fmaf(sg, bf16_hi(w.z), acc[5]);
-        acc[6] = fmaf(sg, bf16_lo(w.w), acc[6]);
-        acc[7] = fmaf(sg, bf16_hi(w.w), acc[7]);
-    }
-}
+// Staged activations of one token chunk.  One token: bf16 pairs (x, -x) per
+// column, so that a compact-table slot value 2*position + negative is directly
+// the element offset from 2*column (no sign arithmetic); several tokens: bf16
+// [column][token].  kPadCols zero columns follow, so that the slots of a
+// corrupt codeword running past the row end still read inside the buffer.
+constexpr int kPadCols = 32;
 
-// One compact-table slot (2*position + negative, 63 = empty) of a codeword
-// whose run starts at column `col`.
 template <int NT>
-__device__ __forceinline__ void apply_slot(uint32_t nz, int col, int cols, float (&acc)[NT], const void* xs,
-                                           bool& bad) {
-    if (nz == (uint32_t)kSlotEmpty) return;
-    const int c = col + (int)(nz >> 1);
-    if (c >= cols) {
-        bad = true;
-        return;
+__device__ __forceinline__ void load_x(const void* xs, int c, bool neg, uint32_t (&w)[(NT + 1) / 2]) {
+    if constexpr (NT == 2) {
+        w[0] = ((const uint32_t*)xs)[c];
+    } else if constexpr (NT == 4) {
+        const uint2 v = ((const uint2*)xs)[c];
+        w[0] = v.x;
+        w[1] = v.y;
+    } else if constexpr (NT == 8) {
+        const uint4 v = ((const uint4*)xs)[c];
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
     }
-    add_x<NT>(c, nz & 1u, acc, xs);
+    const uint32_t flip = neg ? 0x80008000u : 0u;
+#pragma unroll
+    for (int q = 0; q < (NT + 1) / 2; ++q) w[q] ^= flip;
 }
 
 template <bool DICT_SMEM>
@@ -140,6 +125,58 @@ __device__ __forceinline__ void lookup(const GemmArgs& a, const uint16_t* sA, co
     }
 }
 
+// Sum of one codeword's nonzero weights times the staged activations
+// (per token), run starting at column cj.
+template <int NT>
+__device__ __forceinline__ void code_dot(uint32_t ea, uint32_t eb, int cj, const void* xs, float (&t)[NT]) {
+    const uint32_t s0 = (ea >> 4) & 63u, s1 = ea >> 10, s2 = eb & 63u;
+    if constexpr (NT == 1) {
+        const uint16_t* x2 = (const uint16_t*)xs;
+        const int base = 2 * cj;
+        const uint32_t r0 = s0 != 63u ? x2[base + s0] : 0u;
+        const uint32_t r1 = s1 != 63u ? x2[base + s1] : 0u;
+        const uint32_t r2 = s2 != 63u ? x2[base + s2] : 0u;
+        t[0] = (__uint_as_float(r1 << 16) + __uint_as_float(r2 << 16)) + __uint_as_float(r0 << 16);
+    } else {
+        constexpr int W = NT / 2;
+        uint32_t w0[W], w1[W], w2[W];
+#pragma unroll
+        for (int q = 0; q < W; ++q) w0[q] = w1[q] = w2[q] = 0u;
+        if (s0 != 63u) load_x<NT>(xs, cj + (int)(s0 >> 1), s0 & 1u, w0);
+        if (s1 != 63u) load_x<NT>(xs, cj + (int)(s1 >> 1), s1 & 1u, w1);
+        if (s2 != 63u) load_x<NT>(xs, cj + (int)(s2 >> 1), s2 & 1u, w2);
+#pragma unroll
+        for (int q = 0; q < W; ++q) {
+            t[2 * q] = (bf16_lo(w1[q]) + bf16_lo(w2[q])) + bf16_lo(w0[q]);
+            t[2 * q + 1] = (bf16_hi(w1[q]) + bf16_hi(w2[q])) + bf16_hi(w0[q]);
+        }
+    }
+}
+
+// Entry with more than three nonzeros: add its weights from the canonical words.
+template <int NT>
+__device__ void escape_dot(const GemmArgs& a, uint32_t code, int len, int cj, const void* xs, float (&t)[NT]) {
+    const uint32_t c0 = __ldg(a.words + 2 * code), c1 = __ldg(a.words + 2 * code + 1);
+#pragma unroll
+    for (int z = 0; z < NT; ++z) t[z] = 0.0f;
+    for (int q = 0; q < len; ++q) {
+        const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
+        if (s == 0u) continue;
+        if constexpr (NT == 1) {
+            const uint32_t r = ((const uint16_t*)xs)[2 * (cj + q) + (s == 1u ? 1 : 0)];
+            t[0] += __uint_as_float(r << 16);
+        } else {
+            uint32_t w[NT / 2];
+            load_x<NT>(xs, cj + q, s == 1u, w);
+#pragma unroll
+            for (int z = 0; z < NT / 2; ++z) {
+                t[2 * z] += bf16_lo(w[z]);
+                t[2 * z + 1] += bf16_hi(w[z]);
+            }
+        }
+    }
+}
+
 template <int NT>
 __device__ __forceinline__ void flush_row(float* sacc, int row_local, const float (&acc)[NT]) {
 #pragma unroll
@@ -147,93 +184,107 @@ __device__ __forceinline__ void flush_row(float* sacc, int row_local, const floa
 }
 
 // A warp streams the codewords of rows [wr0, wr1) of one matrix as one flat
-// sequence, 8 codewords per lane per window (16-byte loads, the next window
-// held in registers while this one is decoded).  Every row expands to exactly
-// `cols` weights, so the running expansion P of a codeword gives its row and
-// column directly: row = wr0 + P / cols, column = P % cols.  Each lane keeps
-// per-token sums for its current row; when its row changes it flushes them to
-// the shared-memory accumulators, and at the end of a window a segmented
-// warp reduction (lanes are ordered by row) lets the first lane of each row
-// segment add that segment's total.  Rows are owned by one warp, but lanes of
-// the warp may flush the same row, so the adds are shared-memory atomics.
-template <int NT, bool DICT_SMEM>
+// sequence, 8 consecutive codewords per lane per window (16-byte loads, the
+// next window held in registers while this one is decoded).  Every row
+// expands to exactly `cols` weights, so the running expansion P of a codeword
+// gives its row and column: row = P / cols, column = P % cols.  With
+// cols >= 224 the 8 codewords of a lane (at most 224 weights) touch at most
+// two rows, so each lane keeps two sets of per-token sums (its first row and
+// the next); codewords never cross a row.  Narrower matrices take one codeword
+// per lane (CPL = 1), which can never reach a second row.  After a window a lane that crossed
+// adds its first-row sums to the shared accumulators, and a segmented warp
+// reduction (lanes are in row order) lets the first lane of each row segment
+// add that segment's open-row total.  Rows are owned by one warp; lanes of the
+// warp may add to the same row, so the adds are shared-memory atomics.
+template <int CPL>
+__device__ __forceinline__ uint4 load_codes(const uint16_t* codes, uint64_t i) {
+    if constexpr (CPL == 8) return __ldg((const uint4*)(codes + i));
+    else return make_uint4((uint32_t)__ldg(codes + i), 0u, 0u, 0u);
+}
+
+template <int NT, int CPL, bool DICT_SMEM>
 __device__ void stream_rows(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const uint16_t* codes,
-                            uint64_t g_lo, uint64_t g_hi, int cols, int n_rows, const void* xs, float* sacc,
-                            int lane) {
+                            uint64_t g_lo, uint64_t g_hi, int cols, float inv_cols, int n_rows, const void* xs,
+                            float* sacc, int lane) {
+    constexpr int WIN = 32 * CPL;                 // codewords per window
     bool bad = false;
-    float acc[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
     uint32_t P = 0;                               // weights expanded before this window
-    const uint64_t w0 = g_lo & ~7ull;
+    const uint64_t w0 = g_lo & ~(uint64_t)(CPL - 1);
     uint4 nxt = make_uint4(0, 0, 0, 0);
-    if (w0 + 8 * lane < g_hi) nxt = __ldg((const uint4*)(codes + w0 + 8 * lane));
-    for (uint64_t w = w0; w < g_hi; w += 256) {
-        const uint64_t my = w + 8 * (uint64_t)lane;
+    if (w0 + CPL * lane < g_hi) nxt = load_codes<CPL>(codes, w0 + CPL * lane);
+    for (uint64_t w = w0; w < g_hi; w += WIN) {
+        const uint64_t my = w + CPL * (uint64_t)lane;
         const uint4 cur = nxt;
-        if (my + 256 < g_hi) nxt = __ldg((const uint4*)(codes + my + 256));
+        if (my + WIN < g_hi) nxt = load_codes<CPL>(codes, my + WIN);
         const uint32_t cw[4] = {cur.x, cur.y, cur.z, cur.w};
-        uint32_t ea[8], eb[8];
+        uint32_t ea[CPL], eb[CPL];
+        int len[CPL];
         int sum = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < CPL; ++j) {
             const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-            const bool valid = my + j >= g_lo && my + j < g_hi;
             ea[j] = (kSlotEmpty << 4) | (kSlotEmpty << 10);
             eb[j] = kSlotEmpty;
-            if (valid) lookup<DICT_SMEM>(a, sA, sB, code, ea[j], eb[j]);
-            sum += (int)(ea[j] & 15u) * 2;
+            if (my + j >= g_lo && my + j < g_hi) lookup<DICT_SMEM>(a, sA, sB, code, ea[j], eb[j]);
+            len[j] = (int)(ea[j] & 15u) * 2;
+            sum += len[j];
         }
         const int incl = warp_incl_scan(sum, lane);
         const uint32_t start = P + (uint32_t)(incl - sum);
-        int row = (int)(start / (uint32_t)cols);
-        int col = (int)(start - (uint32_t)row * (uint32_t)cols);
+        int row = (int)((float)start * inv_cols);
+        if ((uint32_t)row * (uint32_t)cols > start) --row;
+        else if ((uint32_t)(row + 1) * (uint32_t)cols <= start) ++row;
+        const int col = (int)(start - (uint32_t)row * (uint32_t)cols);
+        const int cross = cols - col;             // codewords whose prefix reaches this start the next row
+        // corrupt stream (more than one row boundary in a lane's codewords): skip the
+        // lane's codewords so that no column index can leave the staged buffer
+        const bool ok = col + sum <= 2 * cols;
+        bad |= !ok;
+        float lo[NT], hi[NT];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int len = (int)(ea[j] & 15u) * 2;
-            if (len == 0) continue;
-            if (row >= n_rows) {
-                bad = true;
-                continue;
-            }
-            apply_slot<NT>((ea[j] >> 4) & 63u, col, cols, acc, xs, bad);
-            apply_slot<NT>(ea[j] >> 10, col, cols, acc, xs, bad);
-            apply_slot<NT>(eb[j] & 63u, col, cols, acc, xs, bad);
-            if (eb[j] & 64u) {
-                // more than three nonzeros: walk the canonical entry
+        for (int t = 0; t < NT; ++t) lo[t] = hi[t] = 0.0f;
+        int pre = 0;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const bool second = pre >= cross;
+            const int cj = col + pre - (second ? cols : 0);
+            float t[NT];
+            if (!ok) {
+#pragma unroll
+                for (int z = 0; z < NT; ++z) t[z] = 0.0f;
+            } else if (eb[j] & 64u) {
                 const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-                const uint32_t c0 = __ldg(a.words + 2 * code), c1 = __ldg(a.words + 2 * code + 1);
-                for (int q = 0; q < len; ++q) {
-                    const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
-                    if (s == 1u || s == 2u) apply_slot<NT>(2u * q + (s == 1u ? 1u : 0u), col, cols, acc, xs, bad);
-                }
+                escape_dot<NT>(a, code, len[j], cj, xs, t);
+            } else {
+                code_dot<NT>(ea[j], eb[j], cj, xs, t);
             }
-            col += len;
-            if (col >= cols) {
-                // the run ended this row (codewords never cross a row)
-                if (col > cols) bad = true;
-                flush_row<NT>(sacc, row, acc);
 #pragma unroll
-                for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-                col = 0;
-                ++row;
+            for (int z = 0; z < NT; ++z) {
+                if (second) hi[z] += t[z];
+                else lo[z] += t[z];
             }
+            pre += len[j];
         }
-        // segmented reduction of the lanes' open rows (lanes are in row order)
-        const int r_clamped = min(row, n_rows - 1);
+        const bool crossed = sum > cross;
+        if (crossed && row < n_rows) flush_row<NT>(sacc, row, lo);
+        const int orow = crossed ? row + 1 : row;
+        float v[NT];
+#pragma unroll
+        for (int z = 0; z < NT; ++z) v[z] = crossed ? hi[z] : lo[z];
+        // segmented reduction of the open rows (lanes are in row order)
+        const int rr = min(orow, n_rows - 1);
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-            const int r_from = __shfl_down_sync(QMOE_FULL_MASK, r_clamped, d);
+            const int r_from = __shfl_down_sync(QMOE_FULL_MASK, rr, d);
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const float v = __shfl_down_sync(QMOE_FULL_MASK, acc[t], d);
-                if (lane + d < 32 && r_from == r_clamped) acc[t] += v;
+            for (int z = 0; z < NT; ++z) {
+                const float o = __shfl_down_sync(QMOE_FULL_MASK, v[z], d);
+                if (lane + d < 32 && r_from == rr) v[z] += o;
             }
         }
-        const int r_prev = __shfl_up_sync(QMOE_FULL_MASK, r_clamped, 1);
-        if ((lane == 0 || r_prev != r_clamped) && row < n_rows) flush_row<NT>(sacc, r_clamped, acc);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+        const int r_prev = __shfl_up_sync(QMOE_FULL_MASK, rr, 1);
+        if ((lane == 0 || r_prev != rr) && orow < n_rows) flush_row<NT>(sacc, rr, v);
+        if (row >= n_rows && sum > 0) bad = true;
         P += (uint32_t)__shfl_sync(QMOE_FULL_MASK, incl, 31);
     }
     if (lane == 0 && P != (uint32_t)n_rows * (uint32_t)cols) bad = true;
@@ -259,17 +310,16 @@ __device__ void stage_x(const GemmArgs& a, const Job& job, void* xs, int tid, in
     const int cols = a.m.cols;
     if constexpr (NT == 1) {
         const uint16_t* src = a.x + (size_t)(slot_at(a, job, 0) / a.x_div) * cols;
-        float* d = (float*)xs;
-        for (int c = tid; c < cols; c += nthreads) d[c] = bf16_to_f32(src[c]);
+        uint32_t* d = (uint32_t*)xs;              // (x, -x) as one 32-bit word per column
+        for (int c = tid; c < cols + kPadCols; c += nthreads) {
+            const uint32_t v = c < cols ? (uint32_t)src[c] : 0u;
+            d[c] = v | ((v ^ 0x8000u) << 16);
+        }
     } else {
         uint16_t* d = (uint16_t*)xs;
         for (int t = 0; t < NT; ++t) {
-            if (t < job.n_tok) {
-                const uint16_t* src = a.x + (size_t)(slot_at(a, job, t) / a.x_div) * cols;
-                for (int c = tid; c < cols; c += nthreads) d[c * NT + t] = src[c];
-            } else {
-                for (int c = tid; c < cols; c += nthreads) d[c * NT + t] = 0;
-            }
+            const uint16_t* src = t < job.n_tok ? a.x + (size_t)(slot_at(a, job, t) / a.x_div) * cols : nullptr;
+            for (int c = tid; c < cols + kPadCols; c += nthreads) d[c * NT + t] = (src && c < cols) ? src[c] : 0;
         }
     }
 }
@@ -312,7 +362,7 @@ __device__ __forceinline__ void tile_rows_of(const GemmArgs& a, int tile, Job& j
     r1 = min(a.m.rows, r0 + a.rows_per_tile);
 }
 
-// Warms L2 with the code range of a tile this block will process next.
+// Warms L2 with the code range of a tile this block will process later.
 __device__ void prefetch_tile(const GemmArgs& a, int tile, int n_tiles) {
     if (tile >= n_tiles) return;
     Job job;
@@ -336,7 +386,8 @@ __device__ void prefetch_tile(const GemmArgs& a, int tile, int n_tiles) {
 
 template <int NT, bool DICT_SMEM>
 __device__ void run_tile(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const Job& job, int r0, int r1,
-                         void* xs, float* sacc, int tid, int nthreads, int warp, int nwarps, int lane) {
+                         void* xs, float* sacc, int tid, int nthreads, int warp, int nwarps, int lane, int tile,
+                         int n_tiles) {
     const MatDev& m = a.m;
     stage_x<NT>(a, job, xs, tid, nthreads);
     const int nr = r1 - r0;
@@ -351,10 +402,16 @@ __device__ void run_tile(const GemmArgs& a, const uint16_t* sA, const uint8_t* s
         if (hi < lo) {
             if (lane == 0) set_error(QMOE_EFORMAT);
         } else {
-            stream_rows<NT, DICT_SMEM>(a, sA, sB, m.codes, base + lo, base + hi, m.cols, wr1 - wr0, xs,
-                                       sacc + (wr0 - r0) * NT, lane);
+            if (m.cols >= 8 * QMOE_MAX_RUN)
+                stream_rows<NT, 8, DICT_SMEM>(a, sA, sB, m.codes, base + lo, base + hi, m.cols, a.inv_cols, wr1 - wr0,
+                                              xs, sacc + (wr0 - r0) * NT, lane);
+            else
+                stream_rows<NT, 1, DICT_SMEM>(a, sA, sB, m.codes, base + lo, base + hi, m.cols, a.inv_cols, wr1 - wr0,
+                                              xs, sacc + (wr0 - r0) * NT, lane);
         }
     }
+    // the last warp, usually done first (it has the fewest rows), warms L2 for a later tile
+    if (warp == nwarps - 1 && lane == 0) prefetch_tile(a, tile + 2 * gridDim.x, n_tiles);
     __syncthreads();
     tile_epilogue<NT>(a, job, r0, nr, sacc, tid, nthreads);
     __syncthreads();
@@ -387,15 +444,14 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
     float* sacc = (float*)(xs + a.xs_bytes);
     __syncthreads();
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        if (tid == 0) prefetch_tile(a, tile + 2 * gridDim.x, n_tiles);
         Job job;
         int r0, r1;
         tile_rows_of(a, tile, job, r0, r1);
         switch (nt_class(job.n_tok)) {
-            case 1: run_tile<1, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
-            case 2: run_tile<2, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
-            case 4: run_tile<4, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
-            default: run_tile<8, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane); break;
+            case 1: run_tile<1, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            case 2: run_tile<2, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            case 4: run_tile<4, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            default: run_tile<8, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
         }
     }
 }
@@ -616,23 +672,33 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
 // ------------------------------------------------------------ host side
 int g_sm_count[64];
 
-size_t xs_bytes(int cols, int nt) { return ((nt == 1 ? (size_t)cols * 4 : (size_t)cols * nt * 2) + 15) & ~(size_t)15; }
+// One token: (x, -x) bf16 pairs; several: bf16 [col][token]; plus kPadCols zero columns.
+size_t xs_bytes(int cols, int nt) {
+    const size_t c = (size_t)cols + kPadCols;
+    return ((nt == 1 ? c * 4 : c * nt * 2) + 15) & ~(size_t)15;
+}
 
-size_t tile_smem(int cols, int nt, int rows_per_tile) { return xs_bytes(cols, nt) + (size_t)rows_per_tile * nt * 4; }
+size_t tile_smem(int cols, int nt) { return xs_bytes(cols, nt) + kSaccBytes; }
 
 // Largest token chunk (8, 4, 2, 1) whose staged activations and row sums fit the budget.
-int nt_max_for(int cols, int budget, int rows_per_tile) {
+int nt_max_for(int cols, int budget) {
     for (int nt = 8; nt >= 1; nt >>= 1)
-        if (tile_smem(cols, nt, rows_per_tile) <= (size_t)budget) return nt;
+        if (tile_smem(cols, nt) <= (size_t)budget) return nt;
     return 0;
 }
 
-// Rows per tile of the L1/L2-dictionary variant: enough tiles to fill the GPU.
-int rows_per_tile_small(int rows, long long n_jobs) {
-    const long long want = 2LL * qmoe::sm_count();
-    long long rpt = (long long)rows * std::max(1LL, n_jobs) / want;
-    rpt = std::max(8LL, std::min(64LL, rpt / 8 * 8));
-    return (int)rpt;
+// Rows per tile: as many as the row-sum buffer holds for nt tokens, split evenly,
+// a multiple of the warp count; at least `min_tiles` tiles when given.
+int rows_per_tile_for(int rows, int nt, int nwarps, long long n_jobs, long long min_tiles) {
+    int cap = kSaccBytes / (4 * nt);
+    if (min_tiles > 0) {
+        const long long per_job = (min_tiles + std::max(1LL, n_jobs) - 1) / std::max(1LL, n_jobs);
+        cap = (int)std::max<long long>(nwarps, std::min<long long>(cap, (rows + per_job - 1) / per_job));
+    }
+    const int n = (rows + cap - 1) / cap;
+    int rpt = (rows + n - 1) / n;
+    rpt = (rpt + nwarps - 1) / nwarps * nwarps;
+    return std::min(rpt, cap / nwarps * nwarps > 0 ? cap / nwarps * nwarps : nwarps);
 }
 
 bool valid_set(const qmoe_matrix_set* s) {
@@ -660,7 +726,8 @@ int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaS
     a.rows_per_tile = rows_per_tile;
     a.row_tiles = (a.m.rows + rows_per_tile - 1) / rows_per_tile;
     a.xs_bytes = (int)xs_bytes(a.m.cols, nt_max);
-    const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + tile_smem(a.m.cols, nt_max, rows_per_tile);
+    a.inv_cols = 1.0f / (float)a.m.cols;
+    const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + tile_smem(a.m.cols, nt_max);
     if (smem > (size_t)kSmemMax) return qmoe::fail(QMOE_EUNSUPPORTED, "dict_gemm: tile does not fit in shared memory");
     if (dict_smem) {
         int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<true>,
@@ -739,7 +806,7 @@ extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* 
     if (T < 0) return fail(QMOE_EINVAL, "qmoe_expert_matvec: T < 0");
     if (T == 0) return QMOE_OK;
     if (!x_bf16 || !y) return fail(QMOE_EINVAL, "qmoe_expert_matvec: NULL x or y");
-    const int nt_max = nt_max_for(mat->cols, kBudgetGlobalDict, 64);
+    const int nt_max = nt_max_for(mat->cols, kBudgetGlobalDict);
     if (!nt_max) return fail(QMOE_EUNSUPPORTED, "qmoe_expert_matvec: cols too large");
     GemmArgs a{};
     a.dictA = (const uint16_t*)dict->compact;
@@ -755,7 +822,7 @@ extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* 
     a.y_is_f32 = y_is_f32 ? 1 : 0;
     a.out = y;
     const long long jobs = (T + nt_max - 1) / nt_max;
-    const int rpt = rows_per_tile_small(mat->rows, jobs);
+    const int rpt = rows_per_tile_for(mat->rows, nt_max, kThreadsGlobalDict / 32, jobs, 2LL * qmoe::sm_count());
     return launch_gemm(a, false, nt_max, rpt, (cudaStream_t)stream, jobs * ((mat->rows + rpt - 1) / rpt));
 }
 
@@ -842,9 +909,11 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     const long long slots = (long long)T * k;
     const bool big = slots >= 16;
     const int budget = big ? kBudgetSmemDict : kBudgetGlobalDict;
-    const int rpt_wi = big ? kRowsSmemDict : rows_per_tile_small(d_ff, slots);
-    const int rpt_wo = big ? kRowsSmemDict : rows_per_tile_small(d_model, slots);
-    const int nt_wi = nt_max_for(d_model, budget, rpt_wi), nt_wo = nt_max_for(d_ff, budget, rpt_wo);
+    const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
+    const int nw = (big ? kThreadsSmemDict : kThreadsGlobalDict) / 32;
+    const long long min_tiles = big ? 0 : 2LL * qmoe::sm_count();
+    const int rpt_wi = nt_wi ? rows_per_tile_for(d_ff, nt_wi, nw, slots, min_tiles) : 0;
+    const int rpt_wo = nt_wo ? rows_per_tile_for(d_model, nt_wo, nw, slots, min_tiles) : 0;
     if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
     cudaStream_t st = (cudaStream_t)stream;
     qmoe::phase_event(0, st);

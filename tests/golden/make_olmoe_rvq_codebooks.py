@@ -1,0 +1,47 @@
+"""Writes olmoe_rvq_codebooks.npy: the OLMoE-shaped layer's two fp16 RVQ codebooks.
+
+Calls only the oracle (and the seeded generators).  One codebook pair serves the
+whole layer ("a single global codebook", Quantization as Cache Amplification,
+section "Codec"): k-means (256 centroids, 25 Lloyd iterations or stable
+assignments, lowest-index ties, empty clusters keep their centroid) on a seeded
+pool of 2**17 8-dim vectors of the row-normalised rotated weights drawn evenly
+from all 64 experts x 3 matrices; stage 2 is fit on the stage-1 residual.
+
+Run from the repository root:  python tests/golden/make_olmoe_rvq_codebooks.py
+"""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from oracle import rvq as R  # noqa: E402
+
+POOL = 1 << 17
+
+
+def main():
+    cfg = synth.OLMOE_RVQ
+    per = POOL // (cfg.E * 3)
+    rng = np.random.default_rng(np.random.SeedSequence([cfg.seed, synth.TAG_KMEANS]))
+    pool = []
+    for e in range(cfg.E):
+        for m in (synth.GATE, synth.UP, synth.DOWN):
+            rows, cols = synth.rvq_matrix_shape(cfg, m)
+            w = synth.rvq_weight(cfg.seed, e, m, rows, cols)
+            so, si = synth.rvq_signs(cfg.seed, e, m, rows, cols)
+            wr = R.rotate_weight(w, so, si)
+            u = R.normalised_vectors(wr, R.row_scale_f16(wr), cfg.vec_dim)
+            pool.append(u[np.sort(rng.choice(u.shape[0], size=per, replace=False))])
+    pool = np.concatenate(pool)
+    cb = R.fit_codebooks(pool, k=cfg.codebook_size, iters=25, seed=cfg.seed)
+    out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "olmoe_rvq_codebooks.npy")
+    np.save(out, cb.astype(np.float16))
+    print(f"wrote {out}: pool {pool.shape}, codebooks {cb.shape}")
+
+
+if __name__ == "__main__":
+    main()
