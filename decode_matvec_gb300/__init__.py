@@ -32,6 +32,7 @@ EXPORTED = [
     "qmoe_bucketise", "qmoe_moe_layer_ws_size", "qmoe_moe_layer", "rvq_expert_matmul_ws_size",
     "rvq_expert_matmul", "rvq_moe_layer_ws_size", "rvq_moe_layer", "rvq_pack", "qmoe_check_status",
     "qmoe_last_error", "qmoe_decode_dense", "rvq_decode_dense", "qmoe_set_phase_events",
+    "qmoe_moe_layer_noalloc",
 ]
 
 
@@ -83,6 +84,7 @@ _sig = {
     "qmoe_decode_dense": [_vp, _vp, _vp, _vp],
     "rvq_decode_dense": [_vp, _vp, _vp],
     "qmoe_set_phase_events": [_vp, _i],
+    "qmoe_moe_layer_noalloc": [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _vp],
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -275,6 +277,16 @@ def qmoe_moe_layer(d: Dictionary, wi: MatrixSet, wo: MatrixSet, x, ids, gates, y
     _check(_lib.qmoe_moe_layer(ctypes.byref(d.c), ctypes.byref(wi.c), ctypes.byref(wo.c), _dptr(x), T, k, _dptr(ids),
                                _dptr(gates), _dptr(y), int(bool(y_is_f32)), _dptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream_ptr(stream)), "qmoe_moe_layer")
+    return y
+
+
+def qmoe_moe_layer_noalloc(d: Dictionary, wi: MatrixSet, wo: MatrixSet, x, ids, gates, y, y_is_f32=True,
+                           stream=None):
+    """qmoe_moe_layer with its scratch in the library's static device buffer (no workspace)."""
+    T, k = ids.shape
+    _check(_lib.qmoe_moe_layer_noalloc(ctypes.byref(d.c), ctypes.byref(wi.c), ctypes.byref(wo.c), _dptr(x), T, k,
+                                       _dptr(ids), _dptr(gates), _dptr(y), int(bool(y_is_f32)), _stream_ptr(stream)),
+           "qmoe_moe_layer_noalloc")
     return y
 
 

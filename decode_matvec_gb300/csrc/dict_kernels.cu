@@ -983,3 +983,59 @@ extern "C" int qmoe_check_status(void* stream) {
     if (b) return fail(b, "device reported an error (RVQ kernels)");
     return QMOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// qmoe_moe_layer_noalloc: the MoE layer with its scratch in a static device array.
+//
+// Some callers cannot allocate device memory at all: code hosted inside
+// another framework that owns every byte of device memory through its own
+// pool, or a serving loop that forbids cudaMalloc/cudaFree after start-up
+// because they can synchronise the device and stall every stream.  For them
+// this entry point takes its scratch from g_noalloc_scratch, a file-scope
+// device array of kNoAllocScratchBytes that every GPU loading this library
+// holds until the process exits.  The caller still provides inputs and
+// outputs.  The array's address is looked up once per device (with that
+// device current) on the first call made on it; that first call should come
+// before any stream capture.  All calls share the array: calls whose work
+// overlaps on the GPU (different streams, or different host threads) race on
+// it and must be serialised by the caller.  Nothing in the scratch has to
+// start at zero: every byte a call reads was written earlier in the same call.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64];
+}  // namespace
+
+extern "C" int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_set* wi, const qmoe_matrix_set* wo,
+                                      const void* x_bf16, int T, int k, const int32_t* ids, const float* gates,
+                                      void* y, int y_is_f32, void* stream) {
+    qmoe::clear_error();
+    if (!wi || !wo) return fail(QMOE_EINVAL, "qmoe_moe_layer_noalloc: NULL matrix set");
+    size_t need = 0;
+    int rc = qmoe_moe_layer_ws_size(wi->count, wi->cols, wi->rows, T, k, &need);
+    if (rc) return rc;
+    if (need > kNoAllocScratchBytes)
+        return fail(QMOE_ECAPACITY, "qmoe_moe_layer_noalloc: this layer call needs " + std::to_string(need) +
+                                        " bytes of scratch; the static scratch holds " +
+                                        std::to_string(kNoAllocScratchBytes) +
+                                        " (use qmoe_moe_layer with a workspace)");
+    int dev = 0;
+    rc = qmoe::cuda_check(cudaGetDevice(&dev), "qmoe_moe_layer_noalloc: cudaGetDevice");
+    if (rc) return rc;
+    if (dev < 0 || dev >= 64) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer_noalloc: device index above 63");
+    void* ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void* p = nullptr;
+            rc = qmoe::cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch),
+                                  "qmoe_moe_layer_noalloc: cudaGetSymbolAddress");
+            if (rc) return rc;
+            g_noalloc_ptr[dev] = p;
+        }
+        ptr = g_noalloc_ptr[dev];
+    }
+    return qmoe_moe_layer(dict, wi, wo, x_bf16, T, k, ids, gates, y, y_is_f32, ptr, kNoAllocScratchBytes, stream);
+}

@@ -222,6 +222,32 @@ int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi,
                    int y_is_f32, void* workspace, size_t ws_bytes,
                    void* stream);
 
+/*
+ * qmoe_moe_layer without a workspace argument.  The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory,
+ * such as code hosted inside a framework that owns all device memory through
+ * its own pool, or serving loops that forbid cudaMalloc/cudaFree after
+ * start-up because those calls can synchronise the device.  It computes
+ * exactly what qmoe_moe_layer computes, with the same arguments minus the
+ * workspace, and allocates nothing: its scratch is a file-scope device array
+ * of 16 MiB (16 << 20 bytes) that every GPU loading the library holds until
+ * the process exits.
+ *  - The first call on a device looks up the array's address on that device
+ *    (with that device current); make that first call before any stream
+ *    capture.
+ *  - Calls whose needs (qmoe_moe_layer_ws_size) exceed 16 MiB are rejected
+ *    with QMOE_ECAPACITY and launch nothing.
+ *  - All calls share the array, which keeps the last call's contents; no
+ *    scratch byte needs to start at zero.  Calls that overlap on the GPU
+ *    (other streams, other host threads) race on the array: serialise them.
+ * Errors: as qmoe_moe_layer, plus ECAPACITY for an oversize call.
+ */
+int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_set* wi,
+                           const qmoe_matrix_set* wo, const void* x_bf16,
+                           int T, int k, const int32_t* ids,
+                           const float* gates, void* y, int y_is_f32,
+                           void* stream);
+
 /* ======================================================================
  * Residual-VQ path
  * ====================================================================== */
