@@ -23,6 +23,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import csv
+import dataclasses
 import hashlib
 import io
 import json
@@ -189,9 +190,9 @@ class DictStep:
         import torch
         self.layer, self.T = layer, T
         # rank r > 0 gets its own independent batch (weak scaling)
-        seed = cfg.seed + 7919 * rank
-        self.logits_host = synth.zipf_logits(seed, T, cfg.E, cfg.zipf_s)
-        self.x_host = synth.activations_bf16(seed, T, cfg.d_model)
+        rcfg = dataclasses.replace(cfg, seed=cfg.seed + 7919 * rank)
+        self.logits_host = synth.layer_logits(rcfg, T)
+        self.x_host = synth.layer_tokens(rcfg, T)
         self.x = torch.from_numpy(self.x_host.view(np.int16).copy()).to(device)
         self.logits = torch.from_numpy(self.logits_host).to(device)
         self.ids = torch.empty((T, 1), dtype=torch.int32, device=device)
@@ -355,49 +356,113 @@ class OracleSampler:
 
 
 # ---------------------------------------------------------------- extra rows
-def extra_rows(layer, device, quick):
-    """Other §-workloads measured in the same run: latency-style and smaller layers."""
+def _time_calls(fn, n=50, warm=5):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1000.0 / n
+
+
+def _dict_layer_row(layer, cfg, T, device, peak, note=""):
+    st = DictStep(layer, cfg, T, 0, device)
+    t = _time_calls(st.run)
+    touched = np.unique(st.ids.cpu().numpy().reshape(-1))
+    sb = layer.stream_bytes(touched)
+    return {"workload": f"{cfg.name} MoE layer (E={cfg.E}, d={cfg.d_model}, f={cfg.d_ff}, p0={cfg.p0}), T={T}{note}",
+            "tokens_per_s": T / t, "ms_per_call": t * 1e3, "touched_experts": int(len(touched)),
+            "stream_bytes": sb, "stream_gbs": sb / t / 1e9, "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak}
+
+
+def _rvq_rows(device, peak):
+    import torch
+    import decode_matvec_gb300 as Q
+    from decode_matvec_gb300.layers import pack_rvq_set
+    cfg = synth.OLMOE_RVQ
+    cb = np.load(os.path.join(ROOT, "tests", "golden", "olmoe_rvq_codebooks.npy")).view(np.uint16)
+    sets = []
+    for m in (synth.GATE, synth.UP, synth.DOWN):
+        rows, cols = synth.rvq_matrix_shape(cfg, m)
+        sets.append(pack_rvq_set(cfg.E, rows, cols, cb, lambda e, m=m, r=rows, c=cols: synth.rvq_weight(cfg.seed, e, m, r, c),
+                                 lambda e, m=m, r=rows, c=cols: synth.rvq_signs(cfg.seed, e, m, r, c), device=device))
+    out = []
+    for T in cfg.tokens:
+        lg = torch.from_numpy(synth.layer_logits(cfg, T)).to(device)
+        x = torch.from_numpy(synth.layer_tokens(cfg, T).view(np.int16).copy()).to(device)
+        ids = torch.empty((T, cfg.top_k), dtype=torch.int32, device=device)
+        gates = torch.empty((T, cfg.top_k), dtype=torch.float32, device=device)
+        y = torch.empty((T, cfg.d_model), dtype=torch.int16, device=device)
+        ws = torch.empty(Q.rvq_moe_layer_ws_size(cfg.E, cfg.d_model, cfg.d_ff, T, cfg.top_k), dtype=torch.uint8,
+                         device=device)
+
+        def step():
+            Q.qmoe_route(lg, cfg.top_k, ids, gates)
+            Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws, y_is_f32=False)
+        t = _time_calls(step)
+        touched = np.unique(ids.cpu().numpy().reshape(-1))
+        per_expert = sum(r * (c // 8) * 2 + r * 2 + r + c for r, c in
+                         (synth.rvq_matrix_shape(cfg, m) for m in (synth.GATE, synth.UP, synth.DOWN)))
+        sb = len(touched) * per_expert + 2 * 256 * 8 * 2
+        out.append({"workload": f"{cfg.name} SwiGLU MoE layer (E={cfg.E}, d={cfg.d_model}, f={cfg.d_ff}, top-8, "
+                                f"2-stage RVQ d=8), T={T}" + (" (tcgen05 path)" if T * cfg.top_k >= 16 else ""),
+                    "tokens_per_s": T / t, "ms_per_call": t * 1e3, "touched_experts": int(len(touched)),
+                    "stream_bytes": int(sb), "stream_gbs": sb / t / 1e9,
+                    "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak})
+    return out
+
+
+def extra_rows(layer, device, peak):
+    """The other workloads, measured in the same run (all bf16 outputs)."""
     import torch
     import decode_matvec_gb300 as Q
     rows = []
-    for T in ((64, 1) if not quick else (1,)):
-        st = DictStep(layer, CFG, T, 0, device)
-        for _ in range(5):
-            st.run()
-        torch.cuda.synchronize()
-        n = 50
-        t = time_steps(st, n, 3, 1) / n
-        ids = st.ids.cpu().numpy().reshape(-1)
-        touched = np.unique(ids)
-        sb = layer.stream_bytes(touched)
-        rows.append({"workload": f"{CFG.name} layer, T={T}", "tokens_per_s": T / t, "ms_per_call": t * 1e3,
-                     "touched_experts": int(len(touched)), "stream_bytes": sb, "stream_gbs": sb / t / 1e9})
-    # single linear layer 1024 x 4096
-    lc = synth.LINEAR_1024x4096
-    lib = native_synth()
-    tern = np.empty((lc.rows, lc.cols), np.int8)
-    lib.synth_ternary_rows(lc.seed, 0, 0, lc.cols, synth.zero_threshold(lc.p0), 0, lc.rows, tern.ctypes.data)
-    words, _ = Q.qmoe_encode_dictionary(lc.p0)
-    codes, off = Q.qmoe_pack(tern, words)
-    d = Q.Dictionary(words, device=device)
-    m = Q.MatrixSet.from_host(codes, off, synth.row_scales(lc.seed, 0, 0, lc.rows), lc.rows, lc.cols, device=device)
-    for T in lc.tokens:
-        x = torch.from_numpy(synth.activations_bf16(lc.seed, T, lc.cols).view(np.int16).copy()).to(device)
-        y = torch.empty((T, lc.rows), dtype=torch.int16, device=device)
-        for _ in range(10):
-            Q.qmoe_expert_matvec(d, m, x, y, y_is_f32=False)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n = 200
-        e0.record()
-        for _ in range(n):
-            Q.qmoe_expert_matvec(d, m, x, y, y_is_f32=False)
-        e1.record()
-        torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) / 1000.0 / n
-        sb = 2 * len(codes) + 4 * len(off) + 2 * lc.rows
-        rows.append({"workload": f"{lc.name}, T={T} (L2-resident: a latency figure)", "tokens_per_s": T / t,
-                     "us_per_call": t * 1e6, "stream_bytes": sb})
+
+    def guarded(fn):
+        try:
+            r = fn()
+            rows.extend(r if isinstance(r, list) else [r])
+        except Exception as exc:  # a failing extra row must not hide the headline line
+            rows.append({"error": f"{type(exc).__name__}: {exc}"})
+
+    for T in (64, 1):
+        guarded(lambda T=T: _dict_layer_row(layer, CFG, T, device, peak,
+                                            " (L2-resident at T=1: a latency figure)" if T == 1 else ""))
+    for cfg in (synth.SWITCH_BASE_128, synth.SWITCH_LARGE_128):
+        def one(cfg=cfg):
+            small = build_dict_layer(cfg, device)
+            r = [_dict_layer_row(small, cfg, T, device, peak, " (layer fits in L2: not an HBM figure)")
+                 for T in cfg.tokens]
+            del small
+            return r
+        guarded(one)
+    guarded(lambda: _rvq_rows(device, peak))
+
+    def linear():
+        lc = synth.LINEAR_1024x4096
+        lib = native_synth()
+        tern = np.empty((lc.rows, lc.cols), np.int8)
+        lib.synth_ternary_rows(lc.seed, 0, 0, lc.cols, synth.zero_threshold(lc.p0), 0, lc.rows, tern.ctypes.data)
+        words, _ = Q.qmoe_encode_dictionary(lc.p0)
+        codes, off = Q.qmoe_pack(tern, words)
+        d = Q.Dictionary(words, device=device)
+        m = Q.MatrixSet.from_host(codes, off, synth.row_scales(lc.seed, 0, 0, lc.rows), lc.rows, lc.cols,
+                                  device=device)
+        out = []
+        for T in lc.tokens:
+            x = torch.from_numpy(synth.activations_bf16(lc.seed, T, lc.cols).view(np.int16).copy()).to(device)
+            y = torch.empty((T, lc.rows), dtype=torch.int16, device=device)
+            t = _time_calls(lambda: Q.qmoe_expert_matvec(d, m, x, y, y_is_f32=False), n=200, warm=10)
+            sb = 2 * len(codes) + 4 * len(off) + 2 * lc.rows
+            out.append({"workload": f"{lc.name}, T={T} (L2-resident: a latency figure)", "tokens_per_s": T / t,
+                        "us_per_call": t * 1e6, "stream_bytes": sb})
+        return out
+    guarded(linear)
     return rows
 
 
@@ -484,7 +549,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = OracleSampler(CFG, T_MAIN).run(budget_s=6.0 if args.quick else 20.0)
     if rank == 0 and not args.quick:
-        line["rows"] = extra_rows(layer, device, args.quick)
+        line["rows"] = extra_rows(layer, device, peak)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

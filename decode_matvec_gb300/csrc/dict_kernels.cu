@@ -86,65 +86,74 @@ struct GemmArgs {
 
 __device__ __forceinline__ int nt_class(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
+// Dynamic shared memory of the expert kernels.  Every region is addressed by a
+// 32-bit byte offset from this symbol, so that the compiler always emits
+// shared-space loads and atomics for the hot loop.
+extern __shared__ __align__(16) unsigned char g_smem[];
+
 // Staged activations of one token chunk.  One token: bf16 pairs (x, -x) per
 // column, so that a compact-table slot value 2*position + negative is directly
 // the element offset from 2*column (no sign arithmetic); several tokens: bf16
-// [column][token].  kPadCols zero columns follow, so that the slots of a
-// corrupt codeword running past the row end still read inside the buffer.
+// [column][token].  kPadCols zero columns follow the row; with cols >= 224 a
+// lane's codeword can never start past column cols-1+... so every slot read
+// stays inside them even for a corrupt stream (see stream_rows).
 constexpr int kPadCols = 32;
 
+struct SmemMap {
+    uint32_t dict_a, dict_b, xs, sacc;
+};
+
 template <int NT>
-__device__ __forceinline__ void load_x(const void* xs, int c, bool neg, uint32_t (&w)[(NT + 1) / 2]) {
+__device__ __forceinline__ void load_x(uint32_t xs, int c, uint32_t flip, uint32_t (&w)[NT / 2]) {
     if constexpr (NT == 2) {
-        w[0] = ((const uint32_t*)xs)[c];
+        w[0] = *(const uint32_t*)(g_smem + xs + 4u * c);
     } else if constexpr (NT == 4) {
-        const uint2 v = ((const uint2*)xs)[c];
+        const uint2 v = *(const uint2*)(g_smem + xs + 8u * c);
         w[0] = v.x;
         w[1] = v.y;
-    } else if constexpr (NT == 8) {
-        const uint4 v = ((const uint4*)xs)[c];
+    } else {
+        const uint4 v = *(const uint4*)(g_smem + xs + 16u * c);
         w[0] = v.x;
         w[1] = v.y;
         w[2] = v.z;
         w[3] = v.w;
     }
-    const uint32_t flip = neg ? 0x80008000u : 0u;
 #pragma unroll
-    for (int q = 0; q < (NT + 1) / 2; ++q) w[q] ^= flip;
+    for (int q = 0; q < NT / 2; ++q) w[q] ^= flip;
 }
 
 template <bool DICT_SMEM>
-__device__ __forceinline__ void lookup(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB,
-                                       uint32_t code, uint32_t& ea, uint32_t& eb) {
+__device__ __forceinline__ void lookup(const GemmArgs& a, const SmemMap& sm, uint32_t code, uint32_t& ea,
+                                       uint32_t& eb) {
     if constexpr (DICT_SMEM) {
-        ea = sA[code];
-        eb = sB[code];
+        ea = *(const uint16_t*)(g_smem + sm.dict_a + 2u * code);
+        eb = *(const uint8_t*)(g_smem + sm.dict_b + code);
     } else {
         ea = __ldg(a.dictA + code);
         eb = __ldg(a.dictB + code);
     }
 }
 
-// Sum of one codeword's nonzero weights times the staged activations
-// (per token), run starting at column cj.
+// Per-token sum of one codeword's weights (at most three nonzeros, from the
+// compact slots) times the staged activations, run starting at column cj.
 template <int NT>
-__device__ __forceinline__ void code_dot(uint32_t ea, uint32_t eb, int cj, const void* xs, float (&t)[NT]) {
+__device__ __forceinline__ void code_dot(uint32_t ea, uint32_t eb, int cj, uint32_t xs, float (&t)[NT]) {
     const uint32_t s0 = (ea >> 4) & 63u, s1 = ea >> 10, s2 = eb & 63u;
     if constexpr (NT == 1) {
-        const uint16_t* x2 = (const uint16_t*)xs;
-        const int base = 2 * cj;
-        const uint32_t r0 = s0 != 63u ? x2[base + s0] : 0u;
-        const uint32_t r1 = s1 != 63u ? x2[base + s1] : 0u;
-        const uint32_t r2 = s2 != 63u ? x2[base + s2] : 0u;
+        const uint32_t base = xs + 4u * (uint32_t)cj;
+        uint32_t r0 = 0, r1 = 0, r2 = 0;
+        if (s0 != 63u) r0 = *(const uint16_t*)(g_smem + base + 2u * s0);
+        if (s1 != 63u) r1 = *(const uint16_t*)(g_smem + base + 2u * s1);
+        if (s2 != 63u) r2 = *(const uint16_t*)(g_smem + base + 2u * s2);
         t[0] = (__uint_as_float(r1 << 16) + __uint_as_float(r2 << 16)) + __uint_as_float(r0 << 16);
     } else {
         constexpr int W = NT / 2;
         uint32_t w0[W], w1[W], w2[W];
 #pragma unroll
         for (int q = 0; q < W; ++q) w0[q] = w1[q] = w2[q] = 0u;
-        if (s0 != 63u) load_x<NT>(xs, cj + (int)(s0 >> 1), s0 & 1u, w0);
-        if (s1 != 63u) load_x<NT>(xs, cj + (int)(s1 >> 1), s1 & 1u, w1);
-        if (s2 != 63u) load_x<NT>(xs, cj + (int)(s2 >> 1), s2 & 1u, w2);
+        if (s0 != 63u) load_x<NT>(xs, cj + (int)(s0 >> 1), (s0 & 1u) * 0x80008000u, w0);
+        if (s1 != 63u) load_x<NT>(xs, cj + (int)(s1 >> 1), (s1 & 1u) * 0x80008000u, w1);
+        if (s2 != 63u) load_x<NT>(xs, cj + (int)(s2 >> 1), (s2 & 1u) * 0x80008000u, w2);
 #pragma unroll
         for (int q = 0; q < W; ++q) {
             t[2 * q] = (bf16_lo(w1[q]) + bf16_lo(w2[q])) + bf16_lo(w0[q]);
@@ -153,21 +162,20 @@ __device__ __forceinline__ void code_dot(uint32_t ea, uint32_t eb, int cj, const
     }
 }
 
-// Entry with more than three nonzeros: add its weights from the canonical words.
+// Entry with more than three nonzeros (its compact slots are all empty): add
+// its weights from the canonical words.
 template <int NT>
-__device__ void escape_dot(const GemmArgs& a, uint32_t code, int len, int cj, const void* xs, float (&t)[NT]) {
+__device__ void escape_dot(const GemmArgs& a, uint32_t code, int len, int cj, uint32_t xs, float (&t)[NT]) {
     const uint32_t c0 = __ldg(a.words + 2 * code), c1 = __ldg(a.words + 2 * code + 1);
-#pragma unroll
-    for (int z = 0; z < NT; ++z) t[z] = 0.0f;
     for (int q = 0; q < len; ++q) {
         const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
         if (s == 0u) continue;
         if constexpr (NT == 1) {
-            const uint32_t r = ((const uint16_t*)xs)[2 * (cj + q) + (s == 1u ? 1 : 0)];
+            const uint32_t r = *(const uint16_t*)(g_smem + xs + 4u * (uint32_t)(cj + q) + (s == 1u ? 2u : 0u));
             t[0] += __uint_as_float(r << 16);
         } else {
             uint32_t w[NT / 2];
-            load_x<NT>(xs, cj + q, s == 1u, w);
+            load_x<NT>(xs, cj + q, s == 1u ? 0x80008000u : 0u, w);
 #pragma unroll
             for (int z = 0; z < NT / 2; ++z) {
                 t[2 * z] += bf16_lo(w[z]);
@@ -178,114 +186,150 @@ __device__ void escape_dot(const GemmArgs& a, uint32_t code, int len, int cj, co
 }
 
 template <int NT>
-__device__ __forceinline__ void flush_row(float* sacc, int row_local, const float (&acc)[NT]) {
+__device__ __forceinline__ void flush_row(uint32_t sacc, int row_local, const float (&acc)[NT]) {
 #pragma unroll
-    for (int t = 0; t < NT; ++t) atomicAdd(sacc + row_local * NT + t, acc[t]);
+    for (int t = 0; t < NT; ++t) atomicAdd((float*)(g_smem + sacc) + row_local * NT + t, acc[t]);
+}
+
+template <int CPL>
+__device__ __forceinline__ uint4 load_codes(const uint16_t* p) {
+    if constexpr (CPL == 8) return __ldg((const uint4*)p);
+    else return make_uint4((uint32_t)__ldg(p), 0u, 0u, 0u);
+}
+
+// One window: CPL consecutive codewords per lane starting at stream index
+// `my`; `valid_lo`/`valid_hi` bound the lane-relative codeword indices that
+// belong to the warp's rows (only edge windows need them).
+template <int NT, int CPL, bool DICT_SMEM, bool EDGE>
+__device__ __forceinline__ void window(const GemmArgs& a, const SmemMap& sm, uint4 cur, int valid_lo, int valid_hi,
+                                       uint32_t& P, int cols, float inv_cols, int n_rows, uint32_t sacc, bool& bad,
+                                       int lane) {
+    const uint32_t cw[4] = {cur.x, cur.y, cur.z, cur.w};
+    uint32_t ea[CPL], eb[CPL];
+    int sum = 0;
+    uint32_t esc = 0;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        if (!EDGE || (j >= valid_lo && j < valid_hi)) {
+            lookup<DICT_SMEM>(a, sm, code, ea[j], eb[j]);
+        } else {
+            ea[j] = (kSlotEmpty << 4) | (kSlotEmpty << 10);
+            eb[j] = kSlotEmpty;
+        }
+        sum += (int)(ea[j] & 15u) * 2;
+        esc |= eb[j];
+    }
+    const int incl = warp_incl_scan(sum, lane);
+    const uint32_t start = P + (uint32_t)(incl - sum);
+    int row = (int)((float)start * inv_cols);
+    if ((uint32_t)row * (uint32_t)cols > start) --row;
+    else if ((uint32_t)(row + 1) * (uint32_t)cols <= start) ++row;
+    const int col = (int)(start - (uint32_t)row * (uint32_t)cols);
+    const int cross = cols - col;                 // prefix from which codewords start in the next row
+    bad |= (col + sum > 2 * cols) | (row >= n_rows && sum > 0);
+    float total[NT], lo[NT];
+#pragma unroll
+    for (int z = 0; z < NT; ++z) total[z] = lo[z] = 0.0f;
+    int pre = 0;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const bool second = pre >= cross;
+        const int cj = second ? col + pre - cols : col + pre;
+        float t[NT];
+        code_dot<NT>(ea[j], eb[j], cj, sm.xs, t);
+#pragma unroll
+        for (int z = 0; z < NT; ++z) {
+            total[z] += t[z];
+            if (!second) lo[z] += t[z];
+        }
+        pre += (int)(ea[j] & 15u) * 2;
+    }
+    if (esc & 64u) {
+        // rare: entries with more than three nonzeros, taken from the canonical words
+        int p2 = 0;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+            const int len = (int)(ea[j] & 15u) * 2;
+            if (eb[j] & 64u) {
+                const bool second = p2 >= cross;
+                const int cj = second ? col + p2 - cols : col + p2;
+                float t[NT];
+#pragma unroll
+                for (int z = 0; z < NT; ++z) t[z] = 0.0f;
+                escape_dot<NT>(a, (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, len, cj, sm.xs, t);
+#pragma unroll
+                for (int z = 0; z < NT; ++z) {
+                    total[z] += t[z];
+                    if (!second) lo[z] += t[z];
+                }
+            }
+            p2 += len;
+        }
+    }
+    // a lane whose codewords reached the next row hands its first-row sums over now
+    const bool crossed = sum > cross;
+    if (crossed && row < n_rows) flush_row<NT>(sacc, row, lo);
+    const int orow = crossed ? row + 1 : row;
+    float v[NT];
+#pragma unroll
+    for (int z = 0; z < NT; ++z) v[z] = crossed ? total[z] - lo[z] : total[z];
+    // segmented reduction of the open rows (lanes are in row order)
+    const int rr = min(orow, n_rows - 1);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int r_from = __shfl_down_sync(QMOE_FULL_MASK, rr, d);
+        const bool take = lane + d < 32 && r_from == rr;
+#pragma unroll
+        for (int z = 0; z < NT; ++z) {
+            const float o = __shfl_down_sync(QMOE_FULL_MASK, v[z], d);
+            if (take) v[z] += o;
+        }
+    }
+    const int r_prev = __shfl_up_sync(QMOE_FULL_MASK, rr, 1);
+    if ((lane == 0 || r_prev != rr) && orow < n_rows) flush_row<NT>(sacc, rr, v);
+    P += (uint32_t)__shfl_sync(QMOE_FULL_MASK, incl, 31);
 }
 
 // A warp streams the codewords of rows [wr0, wr1) of one matrix as one flat
-// sequence, 8 consecutive codewords per lane per window (16-byte loads, the
-// next window held in registers while this one is decoded).  Every row
+// sequence, CPL consecutive codewords per lane per window (16-byte loads; the
+// next window is held in registers while this one is decoded).  Every row
 // expands to exactly `cols` weights, so the running expansion P of a codeword
 // gives its row and column: row = P / cols, column = P % cols.  With
 // cols >= 224 the 8 codewords of a lane (at most 224 weights) touch at most
-// two rows, so each lane keeps two sets of per-token sums (its first row and
-// the next); codewords never cross a row.  Narrower matrices take one codeword
-// per lane (CPL = 1), which can never reach a second row.  After a window a lane that crossed
-// adds its first-row sums to the shared accumulators, and a segmented warp
-// reduction (lanes are in row order) lets the first lane of each row segment
-// add that segment's open-row total.  Rows are owned by one warp; lanes of the
-// warp may add to the same row, so the adds are shared-memory atomics.
-template <int CPL>
-__device__ __forceinline__ uint4 load_codes(const uint16_t* codes, uint64_t i) {
-    if constexpr (CPL == 8) return __ldg((const uint4*)(codes + i));
-    else return make_uint4((uint32_t)__ldg(codes + i), 0u, 0u, 0u);
-}
-
+// two rows; each lane keeps its window total and its first-row part.  A lane
+// that crossed adds its first-row part to the shared accumulators; then a
+// segmented warp reduction (lanes are in row order) lets the first lane of
+// each row segment add that segment's open-row total.  Rows belong to one
+// warp; lanes of the warp may add to the same row, so the adds are
+// shared-memory atomics.  Narrower matrices take one codeword per lane
+// (CPL = 1), which can never reach a second row.  For a corrupt stream every
+// column index still stays below max(cols, 224) + 28, inside the staged
+// buffer and its zero padding; the kernel records QMOE_EFORMAT.
 template <int NT, int CPL, bool DICT_SMEM>
-__device__ void stream_rows(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const uint16_t* codes,
-                            uint64_t g_lo, uint64_t g_hi, int cols, float inv_cols, int n_rows, const void* xs,
-                            float* sacc, int lane) {
-    constexpr int WIN = 32 * CPL;                 // codewords per window
+__device__ void stream_rows(const GemmArgs& a, const SmemMap& sm, const uint16_t* codes, uint64_t g_lo,
+                            uint64_t g_hi, int cols, float inv_cols, int n_rows, uint32_t sacc, int lane) {
+    constexpr int WIN = 32 * CPL;
     bool bad = false;
-    uint32_t P = 0;                               // weights expanded before this window
+    uint32_t P = 0;
     const uint64_t w0 = g_lo & ~(uint64_t)(CPL - 1);
+    const uint16_t* p = codes + w0 + CPL * lane;
+    const int64_t n = (int64_t)(g_hi - w0);       // codewords from w0 to the end of the warp's rows
+    const int head = (int)(g_lo - w0);            // codewords before g_lo in the first window
     uint4 nxt = make_uint4(0, 0, 0, 0);
-    if (w0 + CPL * lane < g_hi) nxt = load_codes<CPL>(codes, w0 + CPL * lane);
-    for (uint64_t w = w0; w < g_hi; w += WIN) {
-        const uint64_t my = w + CPL * (uint64_t)lane;
+    if (CPL * lane < n) nxt = load_codes<CPL>(p);
+    for (int64_t w = 0; w < n; w += WIN) {
         const uint4 cur = nxt;
-        if (my + WIN < g_hi) nxt = load_codes<CPL>(codes, my + WIN);
-        const uint32_t cw[4] = {cur.x, cur.y, cur.z, cur.w};
-        uint32_t ea[CPL], eb[CPL];
-        int len[CPL];
-        int sum = 0;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-            ea[j] = (kSlotEmpty << 4) | (kSlotEmpty << 10);
-            eb[j] = kSlotEmpty;
-            if (my + j >= g_lo && my + j < g_hi) lookup<DICT_SMEM>(a, sA, sB, code, ea[j], eb[j]);
-            len[j] = (int)(ea[j] & 15u) * 2;
-            sum += len[j];
+        const int64_t mine = w + CPL * lane;      // stream index of this lane's first codeword, from w0
+        if (mine + WIN < n) nxt = load_codes<CPL>(p + w + WIN);
+        if (w > 0 && w + WIN <= n) {
+            window<NT, CPL, DICT_SMEM, false>(a, sm, cur, 0, CPL, P, cols, inv_cols, n_rows, sacc, bad, lane);
+        } else {
+            const int64_t lo64 = (int64_t)head - mine, hi64 = n - mine;
+            const int lo = lo64 > 0 ? (int)lo64 : 0;
+            const int hi = hi64 < CPL ? (int)hi64 : CPL;
+            window<NT, CPL, DICT_SMEM, true>(a, sm, cur, lo, hi, P, cols, inv_cols, n_rows, sacc, bad, lane);
         }
-        const int incl = warp_incl_scan(sum, lane);
-        const uint32_t start = P + (uint32_t)(incl - sum);
-        int row = (int)((float)start * inv_cols);
-        if ((uint32_t)row * (uint32_t)cols > start) --row;
-        else if ((uint32_t)(row + 1) * (uint32_t)cols <= start) ++row;
-        const int col = (int)(start - (uint32_t)row * (uint32_t)cols);
-        const int cross = cols - col;             // codewords whose prefix reaches this start the next row
-        // corrupt stream (more than one row boundary in a lane's codewords): skip the
-        // lane's codewords so that no column index can leave the staged buffer
-        const bool ok = col + sum <= 2 * cols;
-        bad |= !ok;
-        float lo[NT], hi[NT];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) lo[t] = hi[t] = 0.0f;
-        int pre = 0;
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const bool second = pre >= cross;
-            const int cj = col + pre - (second ? cols : 0);
-            float t[NT];
-            if (!ok) {
-#pragma unroll
-                for (int z = 0; z < NT; ++z) t[z] = 0.0f;
-            } else if (eb[j] & 64u) {
-                const uint32_t code = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-                escape_dot<NT>(a, code, len[j], cj, xs, t);
-            } else {
-                code_dot<NT>(ea[j], eb[j], cj, xs, t);
-            }
-#pragma unroll
-            for (int z = 0; z < NT; ++z) {
-                if (second) hi[z] += t[z];
-                else lo[z] += t[z];
-            }
-            pre += len[j];
-        }
-        const bool crossed = sum > cross;
-        if (crossed && row < n_rows) flush_row<NT>(sacc, row, lo);
-        const int orow = crossed ? row + 1 : row;
-        float v[NT];
-#pragma unroll
-        for (int z = 0; z < NT; ++z) v[z] = crossed ? hi[z] : lo[z];
-        // segmented reduction of the open rows (lanes are in row order)
-        const int rr = min(orow, n_rows - 1);
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int r_from = __shfl_down_sync(QMOE_FULL_MASK, rr, d);
-#pragma unroll
-            for (int z = 0; z < NT; ++z) {
-                const float o = __shfl_down_sync(QMOE_FULL_MASK, v[z], d);
-                if (lane + d < 32 && r_from == rr) v[z] += o;
-            }
-        }
-        const int r_prev = __shfl_up_sync(QMOE_FULL_MASK, rr, 1);
-        if ((lane == 0 || r_prev != rr) && orow < n_rows) flush_row<NT>(sacc, rr, v);
-        if (row >= n_rows && sum > 0) bad = true;
-        P += (uint32_t)__shfl_sync(QMOE_FULL_MASK, incl, 31);
     }
     if (lane == 0 && P != (uint32_t)n_rows * (uint32_t)cols) bad = true;
     if (__any_sync(QMOE_FULL_MASK, bad) && lane == 0) set_error(QMOE_EFORMAT);
@@ -306,17 +350,17 @@ __device__ __forceinline__ int slot_at(const GemmArgs& a, const Job& job, int i)
 }
 
 template <int NT>
-__device__ void stage_x(const GemmArgs& a, const Job& job, void* xs, int tid, int nthreads) {
+__device__ void stage_x(const GemmArgs& a, const Job& job, uint32_t xs, int tid, int nthreads) {
     const int cols = a.m.cols;
     if constexpr (NT == 1) {
         const uint16_t* src = a.x + (size_t)(slot_at(a, job, 0) / a.x_div) * cols;
-        uint32_t* d = (uint32_t*)xs;              // (x, -x) as one 32-bit word per column
+        uint32_t* d = (uint32_t*)(g_smem + xs);   // (x, -x) as one 32-bit word per column
         for (int c = tid; c < cols + kPadCols; c += nthreads) {
             const uint32_t v = c < cols ? (uint32_t)src[c] : 0u;
             d[c] = v | ((v ^ 0x8000u) << 16);
         }
     } else {
-        uint16_t* d = (uint16_t*)xs;
+        uint16_t* d = (uint16_t*)(g_smem + xs);
         for (int t = 0; t < NT; ++t) {
             const uint16_t* src = t < job.n_tok ? a.x + (size_t)(slot_at(a, job, t) / a.x_div) * cols : nullptr;
             for (int c = tid; c < cols + kPadCols; c += nthreads) d[c * NT + t] = (src && c < cols) ? src[c] : 0;
@@ -326,14 +370,15 @@ __device__ void stage_x(const GemmArgs& a, const Job& job, void* xs, int tid, in
 
 // Scale, activation and store of the tile's rows (threads over rows, per token).
 template <int NT>
-__device__ void tile_epilogue(const GemmArgs& a, const Job& job, int r0, int nr, const float* sacc, int tid,
+__device__ void tile_epilogue(const GemmArgs& a, const Job& job, int r0, int nr, uint32_t sacc, int tid,
                               int nthreads) {
     const int rows = a.m.rows;
     const uint16_t* scale = a.m.scale + (size_t)job.matrix * rows;
+    const float* acc = (const float*)(g_smem + sacc);
     for (int i = tid; i < nr * job.n_tok; i += nthreads) {
         const int t = i / nr, rl = i - t * nr, row = r0 + rl;
         const int slot = slot_at(a, job, t);
-        const float v = f16_to_f32(scale[row]) * sacc[rl * NT + t];
+        const float v = f16_to_f32(scale[row]) * acc[rl * NT + t];
         const size_t o = (size_t)slot * rows + row;
         switch (a.mode) {
             case OUT_PLAIN:
@@ -385,13 +430,12 @@ __device__ void prefetch_tile(const GemmArgs& a, int tile, int n_tiles) {
 }
 
 template <int NT, bool DICT_SMEM>
-__device__ void run_tile(const GemmArgs& a, const uint16_t* sA, const uint8_t* sB, const Job& job, int r0, int r1,
-                         void* xs, float* sacc, int tid, int nthreads, int warp, int nwarps, int lane, int tile,
-                         int n_tiles) {
+__device__ void run_tile(const GemmArgs& a, const SmemMap& sm, const Job& job, int r0, int r1, int tid, int nthreads,
+                         int warp, int nwarps, int lane, int tile, int n_tiles) {
     const MatDev& m = a.m;
-    stage_x<NT>(a, job, xs, tid, nthreads);
+    stage_x<NT>(a, job, sm.xs, tid, nthreads);
     const int nr = r1 - r0;
-    for (int i = tid; i < nr * NT; i += nthreads) sacc[i] = 0.0f;
+    for (int i = tid; i < nr * NT; i += nthreads) ((float*)(g_smem + sm.sacc))[i] = 0.0f;
     __syncthreads();
     const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
     const uint64_t base = m.code_base ? m.code_base[job.matrix] : 0ull;
@@ -402,29 +446,31 @@ __device__ void run_tile(const GemmArgs& a, const uint16_t* sA, const uint8_t* s
         if (hi < lo) {
             if (lane == 0) set_error(QMOE_EFORMAT);
         } else {
+            const uint32_t sacc = sm.sacc + 4u * (uint32_t)((wr0 - r0) * NT);
             if (m.cols >= 8 * QMOE_MAX_RUN)
-                stream_rows<NT, 8, DICT_SMEM>(a, sA, sB, m.codes, base + lo, base + hi, m.cols, a.inv_cols, wr1 - wr0,
-                                              xs, sacc + (wr0 - r0) * NT, lane);
+                stream_rows<NT, 8, DICT_SMEM>(a, sm, m.codes, base + lo, base + hi, m.cols, a.inv_cols, wr1 - wr0,
+                                              sacc, lane);
             else
-                stream_rows<NT, 1, DICT_SMEM>(a, sA, sB, m.codes, base + lo, base + hi, m.cols, a.inv_cols, wr1 - wr0,
-                                              xs, sacc + (wr0 - r0) * NT, lane);
+                stream_rows<NT, 1, DICT_SMEM>(a, sm, m.codes, base + lo, base + hi, m.cols, a.inv_cols, wr1 - wr0,
+                                              sacc, lane);
         }
     }
     // the last warp, usually done first (it has the fewest rows), warms L2 for a later tile
     if (warp == nwarps - 1 && lane == 0) prefetch_tile(a, tile + 2 * gridDim.x, n_tiles);
     __syncthreads();
-    tile_epilogue<NT>(a, job, r0, nr, sacc, tid, nthreads);
+    tile_epilogue<NT>(a, job, r0, nr, sm.sacc, tid, nthreads);
     __syncthreads();
 }
 
 template <bool DICT_SMEM>
 __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
-    extern __shared__ __align__(16) unsigned char smem[];
     const int tid = threadIdx.x, nthreads = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-    const uint16_t* sA = nullptr;
-    const uint8_t* sB = nullptr;
-    unsigned char* xs = smem;
+    SmemMap sm;
+    sm.dict_a = 0;
+    sm.dict_b = kDictA;
+    sm.xs = DICT_SMEM ? (uint32_t)kDictBytes : 0u;
+    sm.sacc = sm.xs + (uint32_t)a.xs_bytes;
     const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
     const int n_tiles = n_jobs * a.row_tiles;
     if (tid == 0) {
@@ -434,24 +480,20 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
     if constexpr (DICT_SMEM) {
         const uint4* srcA = (const uint4*)a.dictA;
         const uint4* srcB = (const uint4*)a.dictB;
-        uint4* dst = (uint4*)smem;
+        uint4* dst = (uint4*)g_smem;
         for (int i = tid; i < kDictA / 16; i += nthreads) dst[i] = __ldg(srcA + i);
         for (int i = tid; i < QMOE_DICT_ENTRIES / 16; i += nthreads) dst[kDictA / 16 + i] = __ldg(srcB + i);
-        sA = (const uint16_t*)smem;
-        sB = (const uint8_t*)(smem + kDictA);
-        xs = smem + kDictBytes;
     }
-    float* sacc = (float*)(xs + a.xs_bytes);
     __syncthreads();
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
         Job job;
         int r0, r1;
         tile_rows_of(a, tile, job, r0, r1);
         switch (nt_class(job.n_tok)) {
-            case 1: run_tile<1, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
-            case 2: run_tile<2, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
-            case 4: run_tile<4, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
-            default: run_tile<8, DICT_SMEM>(a, sA, sB, job, r0, r1, xs, sacc, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            case 1: run_tile<1, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            case 2: run_tile<2, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            case 4: run_tile<4, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            default: run_tile<8, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
         }
     }
 }
