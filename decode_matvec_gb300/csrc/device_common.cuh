@@ -43,10 +43,13 @@ struct Job {
 // Enqueues the single-block planner: per-expert counts, exclusive offsets,
 // the stable slot permutation and, when jobs_a/jobs_b are given, job tables
 // that cut each expert's slots into chunks of nt_a / nt_b tokens
-// (n_jobs[0], n_jobs[1] receive the job counts).
+// (n_jobs[0], n_jobs[1] receive the job counts).  With tc_min > 0 and a
+// jobs_tc table, experts with at least tc_min tokens are left out of the
+// first two tables and cut into chunks of nt_tc tokens in jobs_tc
+// (count in n_jobs[2]).
 int launch_plan(const int32_t* ids, int n_slots, int E, int nt_a, int nt_b, int32_t* counts,
                 int32_t* offsets, int32_t* perm, Job* jobs_a, Job* jobs_b, int* n_jobs,
-                cudaStream_t st);
+                cudaStream_t st, int tc_min = 0, int nt_tc = 1, Job* jobs_tc = nullptr);
 constexpr int kPlanMaxE = 8192;
 
 // Records phase event i on st when the measurement hook is set.

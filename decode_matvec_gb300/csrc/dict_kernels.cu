@@ -25,6 +25,7 @@
 #include <vector>
 
 #include "device_common.cuh"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -39,6 +40,7 @@ constexpr int kSmemMax = 232448;                        // 227 KB opt-in per blo
 constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + row sums, dictionary in SMEM
 constexpr int kBudgetGlobalDict = 56 * 1024;                    // activations + row sums, dictionary via L1/L2
 constexpr int kSaccBytes = 4096;                                // per-tile row sums (rows x tokens x 4 B)
+constexpr int kTcMinTokens = 32;                                // experts this busy use the tensor-core kernel
 constexpr int kThreadsSmemDict = 512;
 constexpr int kThreadsGlobalDict = 256;
 
@@ -498,6 +500,196 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
     }
 }
 
+// ------------------------------------------------------------ tensor-core path for experts with many tokens
+// An expert that receives many tokens is a real dense contraction, and the
+// QMoE page's own suggestion for large token counts is to decompress first and
+// then multiply.  Here the decompression goes to shared memory only: for each
+// 256-weight block of 128 rows, 128 threads expand the rows' codewords into a
+// dense bf16 tile of exact {-1, 0, +1} (one thread per row, nonzeros only,
+// over a zero-filled tile) while the other 128 threads stage the block's
+// activations of up to 64 tokens as bf16; one thread then issues
+// tcgen05.mma (M=128, N=64, K=16, bf16 x bf16 -> fp32 in tensor memory).
+// The row scale is applied in the epilogue, so the product is the same
+// s * sum(+-x) as the CUDA-core kernel, summed in another order.  Each block
+// of ~97 KB of shared memory holds one stage; two blocks per SM overlap one
+// block's decoding with the other's MMAs.  Waits are bounded (QMOE_ETIMEOUT).
+constexpr int kDtcM = 128, kDtcN = 64, kDtcK = 256;
+constexpr int kDtcThreads = 256;
+constexpr uint32_t kDtcLBO = 128, kDtcSBO = (kDtcK / 8) * 128;      // 4096 B
+constexpr int kDtcABytes = kDtcM * kDtcK * 2;                        // 64 KB
+constexpr int kDtcBBytes = kDtcN * kDtcK * 2;                        // 32 KB
+constexpr int kDtcSmem = 1024 + kDtcABytes + kDtcBBytes + 64;
+constexpr uint32_t kDtcIdesc = qmoe_tc::idesc_f16(kDtcM, kDtcN, true, true);
+constexpr uint32_t kDtcSpin = 1u << 20;
+constexpr uint16_t kBf16One = 0x3F80, kBf16MinusOne = 0xBF80;
+
+__device__ __forceinline__ void store_out(const GemmArgs& a, int slot, int row, float v) {
+    const size_t o = (size_t)slot * a.m.rows + row;
+    switch (a.mode) {
+        case OUT_PLAIN:
+            if (a.y_is_f32) ((float*)a.out)[o] = v;
+            else ((uint16_t*)a.out)[o] = f32_to_bf16(v);
+            break;
+        case OUT_RELU_H:
+            ((uint16_t*)a.out)[o] = f32_to_bf16(fmaxf(v, 0.0f));
+            break;
+        case OUT_GATED: {
+            const float g = a.gates[slot] * v;
+            if (a.y_is_f32) ((float*)a.out)[o] = g;
+            else ((uint16_t*)a.out)[o] = f32_to_bf16(g);
+            break;
+        }
+        default:
+            ((float*)a.out)[o] = v;
+            break;
+    }
+}
+
+// One thread expands the codewords of (row, block) into its row of the tile.
+__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, uint32_t lo, uint32_t hi,
+                                                 int blen, unsigned char* A, int rl, bool& bad) {
+    unsigned char* rowbase = A + (rl >> 3) * kDtcSBO + (rl & 7) * 16;
+    int col = 0;
+    for (uint32_t i = lo; i < hi; ++i) {
+        const uint32_t code = __ldg(codes + i);
+        const uint32_t ea = __ldg(a.dictA + code), eb = __ldg(a.dictB + code);
+        const int len = (int)(ea & 15u) * 2;
+        if (col + len > blen) {
+            bad = true;
+            break;
+        }
+        if (eb & 64u) {
+            const uint32_t c0 = __ldg(a.words + 2 * code), c1 = __ldg(a.words + 2 * code + 1);
+            for (int q = 0; q < len; ++q) {
+                const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
+                if (s) {
+                    const int c = col + q;
+                    *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) = s == 1u ? kBf16MinusOne : kBf16One;
+                }
+            }
+        } else {
+            const uint32_t sl[3] = {(ea >> 4) & 63u, ea >> 10, eb & 63u};
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                if (sl[k] != 63u) {
+                    const int c = col + (int)(sl[k] >> 1);
+                    *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) = (sl[k] & 1u) ? kBf16MinusOne : kBf16One;
+                }
+            }
+        }
+        col += len;
+    }
+    if (col != blen) bad = true;
+}
+
+__global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs a) {
+    using namespace qmoe_tc;
+    unsigned char* smem = (unsigned char*)(((uintptr_t)g_smem + 1023) & ~(uintptr_t)1023);
+    unsigned char* A = smem;
+    unsigned char* B = smem + kDtcABytes;
+    uint64_t* bar = (uint64_t*)(B + kDtcBBytes);
+    uint32_t* tmem_slot = (uint32_t*)(bar + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const MatDev& m = a.m;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kDtcN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    uint32_t phase = 0;
+    bool timed_out = false, bad = false;
+    const int n_jobs = *a.n_jobs_dev;
+    const int n_tiles = n_jobs * a.row_tiles;
+    for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+        const Job job = a.jobs[tile / a.row_tiles];
+        const int r0 = (tile % a.row_tiles) * kDtcM;
+        const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
+        const uint16_t* codes = m.codes + (m.code_base ? m.code_base[job.matrix] : 0ull);
+        for (int b = 0; b < m.nb; ++b) {
+            const int blen = min(kDtcK, m.cols - b * kDtcK);
+            // zero the weight tile (16 bytes per store)
+            for (int i = tid; i < kDtcABytes / 16; i += kDtcThreads) ((uint4*)A)[i] = make_uint4(0, 0, 0, 0);
+            __syncthreads();
+            if (tid < kDtcM) {
+                const int row = r0 + tid;
+                if (row < m.rows)
+                    decode_row_block(a, codes, off[(size_t)row * m.nb + b], off[(size_t)row * m.nb + b + 1], blen, A,
+                                     tid, bad);
+            } else {
+                // activations: 64 tokens x 256 columns, 8 columns (16 bytes) per chunk
+                for (int q = tid - kDtcM; q < kDtcN * (kDtcK / 8); q += kDtcThreads - kDtcM) {
+                    const int n = q / (kDtcK / 8), c8 = q % (kDtcK / 8);
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (n < job.n_tok && c8 * 8 < blen) {
+                        const int slot = a.slots[job.slot_begin + n];
+                        v = __ldg((const uint4*)(a.x + (size_t)(slot / a.x_div) * m.cols + b * kDtcK + c8 * 8));
+                    }
+                    *(uint4*)(B + (n >> 3) * kDtcSBO + c8 * kDtcLBO + (n & 7) * 16) = v;
+                }
+            }
+            fence_async_shared();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+                const int ksteps = (blen + 15) / 16;
+                for (int k = 0; k < ksteps; ++k)
+                    mma_f16(tmem, umma_desc(a0 + k * 2 * kDtcLBO, kDtcLBO, kDtcSBO),
+                            umma_desc(b0 + k * 2 * kDtcLBO, kDtcLBO, kDtcSBO), kDtcIdesc, b > 0 || k > 0);
+                mma_commit(bar);
+            }
+            // the tiles are rewritten by the next block: wait for these MMAs
+            if (!mbar_wait(bar, phase & 1u, kDtcSpin)) timed_out = true;
+            ++phase;
+            if (__syncthreads_or(timed_out)) {
+                timed_out = true;
+                break;
+            }
+        }
+        if (timed_out) break;
+        tc_fence_after();
+        if (warp < 4) {
+            const int row = r0 + 32 * warp + lane;
+            const float s = row < m.rows ? f16_to_f32(m.scale[(size_t)job.matrix * m.rows + row]) : 0.0f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32u * half, r);
+                if (row < m.rows) {
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) {
+                        const int nn = 32 * half + n;
+                        if (nn < job.n_tok) store_out(a, a.slots[job.slot_begin + nn], row, s * __uint_as_float(r[n]));
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    if (bad) set_error(QMOE_EFORMAT);
+    if (timed_out && tid == 0) set_error(QMOE_ETIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kDtcN);
+}
+
+int launch_dict_tc(GemmArgs a, cudaStream_t st, long long tiles_hint) {
+    int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtcSmem),
+                              "dict tc attr");
+    if (rc) return rc;
+    a.rows_per_tile = kDtcM;
+    a.row_tiles = (a.m.rows + kDtcM - 1) / kDtcM;
+    const long long grid = std::max(1LL, std::min(tiles_hint, (long long)qmoe::sm_count() * 2));
+    dict_tc_kernel<<<(unsigned)grid, kDtcThreads, kDtcSmem, st>>>(a);
+    return qmoe::launch_check("dict_tc_kernel");
+}
+
 // ------------------------------------------------------------ decode (test)
 __global__ void decode_dense_kernel(const uint32_t* __restrict__ words, MatDev m, float* __restrict__ out) {
     const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
@@ -613,10 +805,11 @@ __device__ int block_excl_scan(int v, int* sbuf) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ ids, int n_slots, int E,
-                                                            int nt_a, int nt_b, int32_t* __restrict__ counts,
+                                                            int nt_a, int nt_b, int tc_min, int nt_tc,
+                                                            int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                                             Job* __restrict__ jobs_a, Job* __restrict__ jobs_b,
-                                                            int* __restrict__ n_jobs) {
+                                                            Job* __restrict__ jobs_tc, int* __restrict__ n_jobs) {
     __shared__ int hist[kPlanMaxE];
     __shared__ int sbuf[32];
     __shared__ int carry;
@@ -670,15 +863,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     }
     __syncthreads();
     if (!jobs_a) return;
-    // job tables: chunks of nt tokens per expert, in expert order
-    for (int which = 0; which < 2; ++which) {
-        const int nt = which == 0 ? nt_a : nt_b;
-        Job* jobs = which == 0 ? jobs_a : jobs_b;
+    // job tables in expert order: chunks of nt tokens of the experts each kernel takes
+    // (experts with at least tc_min tokens go to the tensor-core kernel when tc_min > 0)
+    for (int which = 0; which < 3; ++which) {
+        const int nt = which == 0 ? nt_a : which == 1 ? nt_b : nt_tc;
+        Job* jobs = which == 0 ? jobs_a : which == 1 ? jobs_b : jobs_tc;
+        if (which == 2 && !jobs_tc) {
+            if (tid == 0) n_jobs[2] = 0;
+            break;
+        }
         if (tid == 0) carry = 0;
         __syncthreads();
         for (int base = 0; base < E; base += blockDim.x) {
             const int e = base + tid;
-            const int c = e < E ? counts[e] : 0;
+            int c = e < E ? counts[e] : 0;
+            const bool tc = tc_min > 0 && c >= tc_min;
+            if (tc != (which == 2)) c = 0;
             const int nj = (c + nt - 1) / nt;
             const int ex = block_excl_scan(nj, sbuf);
             const int first = carry + ex;
@@ -804,8 +1004,10 @@ int sm_count() {
 }
 
 int launch_plan(const int32_t* ids, int n_slots, int E, int nt_a, int nt_b, int32_t* counts, int32_t* offsets,
-                int32_t* perm, Job* jobs_a, Job* jobs_b, int* n_jobs, cudaStream_t st) {
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(ids, n_slots, E, nt_a, nt_b, counts, offsets, perm, jobs_a, jobs_b, n_jobs);
+                int32_t* perm, Job* jobs_a, Job* jobs_b, int* n_jobs, cudaStream_t st, int tc_min, int nt_tc,
+                Job* jobs_tc) {
+    plan_kernel<<<1, kPlanThreads, 0, st>>>(ids, n_slots, E, nt_a, nt_b, tc_min, nt_tc, counts, offsets, perm, jobs_a,
+                                            jobs_b, jobs_tc, n_jobs);
     return launch_check("plan_kernel");
 }
 
@@ -887,6 +1089,7 @@ struct MoeWs {
     int32_t* perm;
     Job* jobs_a;
     Job* jobs_b;
+    Job* jobs_tc;
     int* n_jobs;
     uint16_t* h;
     float* o;
@@ -909,7 +1112,8 @@ MoeWs moe_ws_layout(void* base, int E, int d_model, int d_ff, int T, int k) {
     w.perm = (int32_t*)take(sizeof(int32_t) * std::max<size_t>(slots, 1));
     w.jobs_a = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
     w.jobs_b = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
-    w.n_jobs = (int*)take(sizeof(int) * 2);
+    w.jobs_tc = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
+    w.n_jobs = (int*)take(sizeof(int) * 4);
     w.h = (uint16_t*)take(sizeof(uint16_t) * slots * d_ff);
     w.o = k > 1 ? (float*)take(sizeof(float) * slots * d_model) : nullptr;
     w.bytes = off;
@@ -958,9 +1162,11 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     const int rpt_wo = nt_wo ? rows_per_tile_for(d_model, nt_wo, nw, slots, min_tiles) : 0;
     if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
     cudaStream_t st = (cudaStream_t)stream;
+    // experts with at least kTcMinTokens tokens take the tensor-core kernel
+    const bool use_tc = big && slots >= kTcMinTokens && d_model % 8 == 0 && d_ff % 8 == 0;
     qmoe::phase_event(0, st);
     int rc = qmoe::launch_plan(ids, (int)slots, E, nt_wi, nt_wo, w.counts, w.offsets, w.perm, w.jobs_a, w.jobs_b,
-                               w.n_jobs, st);
+                               w.n_jobs, st, use_tc ? kTcMinTokens : 0, kDtcN, use_tc ? w.jobs_tc : nullptr);
     if (rc) return rc;
     qmoe::phase_event(1, st);
     GemmArgs a{};
@@ -981,6 +1187,12 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     a.out = w.h;
     rc = launch_gemm(a, big, nt_wi, rpt_wi, st, slots * ((d_ff + rpt_wi - 1) / rpt_wi));
     if (rc) return rc;
+    if (use_tc) {
+        GemmArgs t = a;
+        t.jobs = w.jobs_tc;
+        t.n_jobs_dev = w.n_jobs + 2;
+        if ((rc = launch_dict_tc(t, st, 2LL * qmoe::sm_count()))) return rc;
+    }
     qmoe::phase_event(2, st);
     // wo: o[slot] = Wo h[slot]; gated straight into y when k == 1
     a.m = to_dev(wo);
@@ -992,6 +1204,12 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     a.out = k == 1 ? y : (void*)w.o;
     rc = launch_gemm(a, big, nt_wo, rpt_wo, st, slots * ((d_model + rpt_wo - 1) / rpt_wo));
     if (rc) return rc;
+    if (use_tc) {
+        GemmArgs t = a;
+        t.jobs = w.jobs_tc;
+        t.n_jobs_dev = w.n_jobs + 2;
+        if ((rc = launch_dict_tc(t, st, 2LL * qmoe::sm_count()))) return rc;
+    }
     qmoe::phase_event(3, st);
     if (k > 1) {
         const size_t n = (size_t)T * d_model;

@@ -653,7 +653,7 @@ RvqMoeWs rvq_moe_layout(void* base, int E, int d_model, int d_ff, int T, int k) 
     w.perm = (int32_t*)take(sizeof(int32_t) * std::max<size_t>(slots, 1));
     w.jobs_a = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
     w.jobs_b = (Job*)take(sizeof(Job) * std::max<size_t>(slots, 1));
-    w.n_jobs = (int*)take(sizeof(int) * 2);
+    w.n_jobs = (int*)take(sizeof(int) * 4);
     w.expert_of = nullptr;
     w.xg = (float*)take(sizeof(float) * slots * d_model);
     w.xu = (float*)take(sizeof(float) * slots * d_model);
