@@ -42,6 +42,7 @@ import synth  # noqa: E402
 
 CFG = synth.SWITCH_C2048
 T_MAIN = 4096
+TC_MIN_TOKENS = 32      # experts with this many tokens take the tensor-core kernel
 METRIC = "MoE-layer tokens/s and compressed-stream HBM GB/s (% of GB300 peak) at 1 GPU"
 UNIT = "tokens/s"
 WORKLOAD = (f"{CFG.name} MoE FFN layer: E={CFG.E}, d_model={CFG.d_model}, d_ff={CFG.d_ff}, T={T_MAIN} bf16 tokens, "
@@ -209,7 +210,7 @@ class DictStep:
         Q.qmoe_moe_layer(L.dictionary, L.wi, L.wo, self.x, self.ids, self.gates, self.y, self.ws, y_is_f32=False,
                          stream=stream)
 
-    launches_per_step = 4   # route, plan, wi kernel, wo kernel
+    launches_per_step = 6   # route, plan, wi CUDA-core + tensor-core kernels, wo CUDA-core + tensor-core kernels
 
 
 def time_steps(step, K, W, world):
@@ -256,12 +257,14 @@ def time_phases(step, K):
         rec.append((r0, r1, ev))
     Q.qmoe_set_phase_events(None)
     torch.cuda.synchronize()
-    out = {"route": 0.0, "plan": 0.0, "wi": 0.0, "wo": 0.0}
+    out = {"route": 0.0, "plan": 0.0, "wi": 0.0, "wi_tc": 0.0, "wo": 0.0, "wo_tc": 0.0}
     for r0, r1, ev in rec:
         out["route"] += r0.elapsed_time(r1) / 1000.0
         out["plan"] += ev[0].elapsed_time(ev[1]) / 1000.0
         out["wi"] += ev[1].elapsed_time(ev[2]) / 1000.0
-        out["wo"] += ev[2].elapsed_time(ev[3]) / 1000.0
+        out["wi_tc"] += ev[2].elapsed_time(ev[3]) / 1000.0
+        out["wo"] += ev[3].elapsed_time(ev[4]) / 1000.0
+        out["wo_tc"] += ev[4].elapsed_time(ev[5]) / 1000.0
     return {k: v / K for k, v in out.items()}
 
 
@@ -475,7 +478,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="skip the extra rows and shorten the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="profiling case: keep only this many experts of the c2048-shaped layer")
+    ap.add_argument("--tokens", type=int, default=None, help="profiling case: token batch size")
     args = ap.parse_args()
+    global CFG, T_MAIN, WORKLOAD
+    if args.experts or args.tokens:
+        CFG = dataclasses.replace(CFG, E=args.experts or CFG.E)
+        T_MAIN = args.tokens or T_MAIN
+        WORKLOAD = WORKLOAD.replace("E=2048", f"E={CFG.E}").replace("T=4096", f"T={T_MAIN}") + \
+            " (reduced profiling case)"
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     rank, world, local = dist_setup()
@@ -515,13 +527,22 @@ def main():
     touched = np.unique(ids)
     phases = time_phases(step, min(args.steps, 50))
     stream_bytes = layer.stream_bytes(touched)
-    compact = 3 * 65536
-    x_bytes, h_bytes, y_bytes = T_MAIN * CFG.d_model * 2, T_MAIN * CFG.d_ff * 2, T_MAIN * CFG.d_model * 2
-    alg_wi = sum(layer.wi_host.expert_bytes(e) for e in touched) + x_bytes + h_bytes + compact
-    alg_wo = sum(layer.wo_host.expert_bytes(e) for e in touched) + h_bytes + y_bytes + compact
-    t_k = phases["wi"] + phases["wo"]
+    counts = np.bincount(ids, minlength=CFG.E)
+    # experts with >= 32 tokens run on the tensor-core kernel (large launches only)
+    hot = counts >= TC_MIN_TOKENS if T_MAIN >= TC_MIN_TOKENS else np.zeros(CFG.E, bool)
+    kern = {}
+    for name, sel, secs_k in (("dict_gemm_kernel", (counts > 0) & ~hot, phases["wi"] + phases["wo"]),
+                              ("dict_tc_kernel", hot, phases["wi_tc"] + phases["wo_tc"])):
+        ex = np.nonzero(sel)[0]
+        n_tok = int(counts[ex].sum())
+        act = n_tok * (2 * CFG.d_model * 2 + 2 * CFG.d_ff * 2)     # x in, h out, h in, y out
+        b = layer.stream_bytes(ex) + act + (2 * 3 * 65536 if name == "dict_gemm_kernel" else 0)
+        kern[name] = {"experts": int(len(ex)), "tokens": n_tok, "launches_per_step": 2,
+                      "ms_per_step": secs_k * 1e3, "algorithmic_bytes_per_step": int(b),
+                      "achieved_gbs": (b / secs_k / 1e9) if secs_k > 0 else None}
+    dom = max(kern, key=lambda k: kern[k]["ms_per_step"])
     peak, peak_kind = hbm_peak()
-    achieved = (alg_wi + alg_wo) / t_k / 1e9
+    achieved = kern[dom]["achieved_gbs"]
     e2e_s, bi, bo = time_e2e(step, max(10, args.steps // 4), 3)
 
     line = {
@@ -535,12 +556,11 @@ def main():
                    "parallelism": f"{world} independent replicas (one token batch per GPU)"},
         "stream_gbs": stream_bytes / (secs / args.steps) / 1e9,
         "stream_pct_of_hbm_peak": 100.0 * stream_bytes / (secs / args.steps) / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": "dict_gemm_kernel (wi and wo launches)",
-                     "achieved": achieved, "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)"
-                     if peak_kind == "measured" else "fallback", "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": kernel_traffic("decode_matvec_gb300/csrc/dict_kernels.cu", "dict_gemm_kernel"),
-                     "algorithmic_bytes_per_step": alg_wi + alg_wo,
-                     "kernel_ms": {k: v * 1e3 for k, v in phases.items()}},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": "measured (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": kernel_traffic("decode_matvec_gb300/csrc/dict_kernels.cu", dom),
+                     "kernels": kern, "phase_ms": {k: v * 1e3 for k, v in phases.items()}},
         "e2e": {"value": T_MAIN / e2e_s, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
         "gpu_launches": DictStep.launches_per_step * args.steps,
         "clocks": clk.summary(),

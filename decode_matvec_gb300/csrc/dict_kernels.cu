@@ -39,7 +39,7 @@ constexpr int kSlotEmpty = 63;
 constexpr int kSmemMax = 232448;                        // 227 KB opt-in per block
 constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + row sums, dictionary in SMEM
 constexpr int kBudgetGlobalDict = 56 * 1024;                    // activations + row sums, dictionary via L1/L2
-constexpr int kSaccBytes = 4096;                                // per-tile row sums (rows x tokens x 4 B)
+constexpr int kSaccBytes = 8192;                                // per-tile row sums (rows x tokens x 4 B)
 constexpr int kTcMinTokens = 32;                                // experts this busy use the tensor-core kernel
 constexpr int kThreadsSmemDict = 512;
 constexpr int kThreadsGlobalDict = 256;
@@ -324,6 +324,10 @@ __device__ void stream_rows(const GemmArgs& a, const SmemMap& sm, const uint16_t
         const uint4 cur = nxt;
         const int64_t mine = w + CPL * lane;      // stream index of this lane's first codeword, from w0
         if (mine + WIN < n) nxt = load_codes<CPL>(p + w + WIN);
+        // keep about four windows of this warp's stream in flight towards L2
+        // (one prefetch per 128-byte line)
+        if (CPL == 8 && (lane & 7) == 0 && mine + 4 * WIN < n)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p + w + 4 * WIN));
         if (w > 0 && w + WIN <= n) {
             window<NT, CPL, DICT_SMEM, false>(a, sm, cur, 0, CPL, P, cols, inv_cols, n_rows, sacc, bad, lane);
         } else {
@@ -351,21 +355,39 @@ __device__ __forceinline__ int slot_at(const GemmArgs& a, const Job& job, int i)
     return a.slots ? a.slots[job.slot_begin + i] : job.slot_begin + i;
 }
 
+// Loads of G columns per thread are issued together, then stored: the
+// staging costs a couple of memory round trips rather than one per column.
 template <int NT>
 __device__ void stage_x(const GemmArgs& a, const Job& job, uint32_t xs, int tid, int nthreads) {
-    const int cols = a.m.cols;
-    if constexpr (NT == 1) {
-        const uint16_t* src = a.x + (size_t)(slot_at(a, job, 0) / a.x_div) * cols;
-        uint32_t* d = (uint32_t*)(g_smem + xs);   // (x, -x) as one 32-bit word per column
-        for (int c = tid; c < cols + kPadCols; c += nthreads) {
-            const uint32_t v = c < cols ? (uint32_t)src[c] : 0u;
-            d[c] = v | ((v ^ 0x8000u) << 16);
+    constexpr int G = 8;
+    const int cols = a.m.cols, total = cols + kPadCols;
+    const uint16_t* src[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+        src[t] = t < job.n_tok ? a.x + (size_t)(slot_at(a, job, t) / a.x_div) * cols : nullptr;
+    for (int c0 = tid; c0 < total; c0 += nthreads * G) {
+        uint32_t v[G][NT];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int c = c0 + g * nthreads;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) v[g][t] = (src[t] && c < cols) ? (uint32_t)__ldg(src[t] + c) : 0u;
         }
-    } else {
-        uint16_t* d = (uint16_t*)(g_smem + xs);
-        for (int t = 0; t < NT; ++t) {
-            const uint16_t* src = t < job.n_tok ? a.x + (size_t)(slot_at(a, job, t) / a.x_div) * cols : nullptr;
-            for (int c = tid; c < cols + kPadCols; c += nthreads) d[c * NT + t] = (src && c < cols) ? src[c] : 0;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int c = c0 + g * nthreads;
+            if (c >= total) break;
+            if constexpr (NT == 1) {
+                // (x, -x) as one 32-bit word per column
+                *(uint32_t*)(g_smem + xs + 4u * c) = v[g][0] | ((v[g][0] ^ 0x8000u) << 16);
+            } else if constexpr (NT == 2) {
+                *(uint32_t*)(g_smem + xs + 4u * c) = v[g][0] | (v[g][1] << 16);
+            } else if constexpr (NT == 4) {
+                *(uint2*)(g_smem + xs + 8u * c) = make_uint2(v[g][0] | (v[g][1] << 16), v[g][2] | (v[g][3] << 16));
+            } else {
+                *(uint4*)(g_smem + xs + 16u * c) = make_uint4(v[g][0] | (v[g][1] << 16), v[g][2] | (v[g][3] << 16),
+                                                              v[g][4] | (v[g][5] << 16), v[g][6] | (v[g][7] << 16));
+            }
         }
     }
 }
@@ -433,9 +455,9 @@ __device__ void prefetch_tile(const GemmArgs& a, int tile, int n_tiles) {
 
 template <int NT, bool DICT_SMEM>
 __device__ void run_tile(const GemmArgs& a, const SmemMap& sm, const Job& job, int r0, int r1, int tid, int nthreads,
-                         int warp, int nwarps, int lane, int tile, int n_tiles) {
+                         int warp, int nwarps, int lane, int prefetch, int n_tiles, bool restage) {
     const MatDev& m = a.m;
-    stage_x<NT>(a, job, sm.xs, tid, nthreads);
+    if (restage) stage_x<NT>(a, job, sm.xs, tid, nthreads);
     const int nr = r1 - r0;
     for (int i = tid; i < nr * NT; i += nthreads) ((float*)(g_smem + sm.sacc))[i] = 0.0f;
     __syncthreads();
@@ -458,7 +480,7 @@ __device__ void run_tile(const GemmArgs& a, const SmemMap& sm, const Job& job, i
         }
     }
     // the last warp, usually done first (it has the fewest rows), warms L2 for a later tile
-    if (warp == nwarps - 1 && lane == 0) prefetch_tile(a, tile + 2 * gridDim.x, n_tiles);
+    if (warp == nwarps - 1 && lane == 0) prefetch_tile(a, prefetch, n_tiles);
     __syncthreads();
     tile_epilogue<NT>(a, job, r0, nr, sm.sacc, tid, nthreads);
     __syncthreads();
@@ -475,9 +497,13 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
     sm.sacc = sm.xs + (uint32_t)a.xs_bytes;
     const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
     const int n_tiles = n_jobs * a.row_tiles;
+    // each block takes a contiguous range of tiles: consecutive tiles of one job
+    // reuse the staged activations
+    const int per_block = (n_tiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per_block, t_end = min(n_tiles, t_begin + per_block);
     if (tid == 0) {
-        prefetch_tile(a, blockIdx.x, n_tiles);
-        prefetch_tile(a, blockIdx.x + gridDim.x, n_tiles);
+        prefetch_tile(a, t_begin, t_end);
+        prefetch_tile(a, t_begin + 1, t_end);
     }
     if constexpr (DICT_SMEM) {
         const uint4* srcA = (const uint4*)a.dictA;
@@ -487,15 +513,19 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
         for (int i = tid; i < QMOE_DICT_ENTRIES / 16; i += nthreads) dst[kDictA / 16 + i] = __ldg(srcB + i);
     }
     __syncthreads();
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    int staged = -1;
+    for (int tile = t_begin; tile < t_end; ++tile) {
         Job job;
         int r0, r1;
         tile_rows_of(a, tile, job, r0, r1);
+        const int j = tile / a.row_tiles;
+        const bool restage = j != staged;
+        staged = j;
         switch (nt_class(job.n_tok)) {
-            case 1: run_tile<1, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
-            case 2: run_tile<2, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
-            case 4: run_tile<4, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
-            default: run_tile<8, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile, n_tiles); break;
+            case 1: run_tile<1, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
+            case 2: run_tile<2, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
+            case 4: run_tile<4, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
+            default: run_tile<8, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
         }
     }
 }
@@ -546,38 +576,53 @@ __device__ __forceinline__ void store_out(const GemmArgs& a, int slot, int row, 
 }
 
 // One thread expands the codewords of (row, block) into its row of the tile.
+// The codewords are read 16 at a time, then all their dictionary entries, so
+// that a block costs a few memory round trips instead of two per codeword.
 __device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, uint32_t lo, uint32_t hi,
                                                  int blen, unsigned char* A, int rl, bool& bad) {
+    constexpr int CH = 16;
     unsigned char* rowbase = A + (rl >> 3) * kDtcSBO + (rl & 7) * 16;
     int col = 0;
-    for (uint32_t i = lo; i < hi; ++i) {
-        const uint32_t code = __ldg(codes + i);
-        const uint32_t ea = __ldg(a.dictA + code), eb = __ldg(a.dictB + code);
-        const int len = (int)(ea & 15u) * 2;
-        if (col + len > blen) {
-            bad = true;
-            break;
-        }
-        if (eb & 64u) {
-            const uint32_t c0 = __ldg(a.words + 2 * code), c1 = __ldg(a.words + 2 * code + 1);
-            for (int q = 0; q < len; ++q) {
-                const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
-                if (s) {
-                    const int c = col + q;
-                    *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) = s == 1u ? kBf16MinusOne : kBf16One;
-                }
-            }
-        } else {
-            const uint32_t sl[3] = {(ea >> 4) & 63u, ea >> 10, eb & 63u};
+    for (uint32_t i0 = lo; i0 < hi; i0 += CH) {
+        uint32_t code[CH], ea[CH], eb[CH];
 #pragma unroll
-            for (int k = 0; k < 3; ++k) {
-                if (sl[k] != 63u) {
-                    const int c = col + (int)(sl[k] >> 1);
-                    *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) = (sl[k] & 1u) ? kBf16MinusOne : kBf16One;
+        for (int k = 0; k < CH; ++k) code[k] = i0 + k < hi ? (uint32_t)__ldg(codes + i0 + k) : 0u;
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            ea[k] = i0 + k < hi ? (uint32_t)__ldg(a.dictA + code[k]) : 0u;
+            eb[k] = i0 + k < hi ? (uint32_t)__ldg(a.dictB + code[k]) : 63u;
+        }
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int len = (int)(ea[k] & 15u) * 2;
+            if (len == 0) continue;
+            if (col + len > blen) {
+                bad = true;
+                break;
+            }
+            if (eb[k] & 64u) {
+                const uint32_t c0 = __ldg(a.words + 2 * code[k]), c1 = __ldg(a.words + 2 * code[k] + 1);
+                for (int q = 0; q < len; ++q) {
+                    const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
+                    if (s) {
+                        const int c = col + q;
+                        *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) = s == 1u ? kBf16MinusOne : kBf16One;
+                    }
+                }
+            } else {
+                const uint32_t sl[3] = {(ea[k] >> 4) & 63u, ea[k] >> 10, eb[k] & 63u};
+#pragma unroll
+                for (int z = 0; z < 3; ++z) {
+                    if (sl[z] != 63u) {
+                        const int c = col + (int)(sl[z] >> 1);
+                        *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) =
+                            (sl[z] & 1u) ? kBf16MinusOne : kBf16One;
+                    }
                 }
             }
+            col += len;
         }
-        col += len;
+        if (bad) break;
     }
     if (col != blen) bad = true;
 }
@@ -620,16 +665,20 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
                     decode_row_block(a, codes, off[(size_t)row * m.nb + b], off[(size_t)row * m.nb + b + 1], blen, A,
                                      tid, bad);
             } else {
-                // activations: 64 tokens x 256 columns, 8 columns (16 bytes) per chunk
+                // activations: 64 tokens x 256 columns in 16-byte asynchronous copies
+                // (zero-filled past the tokens and columns that exist), all in flight at once
                 for (int q = tid - kDtcM; q < kDtcN * (kDtcK / 8); q += kDtcThreads - kDtcM) {
                     const int n = q / (kDtcK / 8), c8 = q % (kDtcK / 8);
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (n < job.n_tok && c8 * 8 < blen) {
-                        const int slot = a.slots[job.slot_begin + n];
-                        v = __ldg((const uint4*)(a.x + (size_t)(slot / a.x_div) * m.cols + b * kDtcK + c8 * 8));
-                    }
-                    *(uint4*)(B + (n >> 3) * kDtcSBO + c8 * kDtcLBO + (n & 7) * 16) = v;
+                    const bool live = n < job.n_tok && c8 * 8 < blen;
+                    const uint16_t* src = a.x;
+                    if (live) src = a.x + (size_t)(a.slots[job.slot_begin + n] / a.x_div) * m.cols + b * kDtcK + c8 * 8;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                                     smem_u32(B + (n >> 3) * kDtcSBO + c8 * kDtcLBO + (n & 7) * 16)),
+                                 "l"(src), "r"(live ? 16 : 0)
+                                 : "memory");
                 }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
             }
             fence_async_shared();
             __syncthreads();
@@ -1187,13 +1236,14 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     a.out = w.h;
     rc = launch_gemm(a, big, nt_wi, rpt_wi, st, slots * ((d_ff + rpt_wi - 1) / rpt_wi));
     if (rc) return rc;
+    qmoe::phase_event(2, st);
     if (use_tc) {
         GemmArgs t = a;
         t.jobs = w.jobs_tc;
         t.n_jobs_dev = w.n_jobs + 2;
         if ((rc = launch_dict_tc(t, st, 2LL * qmoe::sm_count()))) return rc;
     }
-    qmoe::phase_event(2, st);
+    qmoe::phase_event(3, st);
     // wo: o[slot] = Wo h[slot]; gated straight into y when k == 1
     a.m = to_dev(wo);
     a.x = w.h;
@@ -1204,19 +1254,19 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     a.out = k == 1 ? y : (void*)w.o;
     rc = launch_gemm(a, big, nt_wo, rpt_wo, st, slots * ((d_model + rpt_wo - 1) / rpt_wo));
     if (rc) return rc;
+    qmoe::phase_event(4, st);
     if (use_tc) {
         GemmArgs t = a;
         t.jobs = w.jobs_tc;
         t.n_jobs_dev = w.n_jobs + 2;
         if ((rc = launch_dict_tc(t, st, 2LL * qmoe::sm_count()))) return rc;
     }
-    qmoe::phase_event(3, st);
     if (k > 1) {
         const size_t n = (size_t)T * d_model;
         combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(w.o, gates, T, k, d_model, y, y_is_f32 ? 1 : 0);
         rc = qmoe::launch_check("combine_kernel");
     }
-    qmoe::phase_event(4, st);
+    qmoe::phase_event(5, st);
     return rc;
 }
 

@@ -333,8 +333,10 @@ int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_out,
  * When `events` is non-NULL, later qmoe_moe_layer and rvq_moe_layer calls in
  * this process record events[i] (cudaEvent_t handles owned by the caller) on
  * their stream at phase boundaries:
- *   qmoe_moe_layer: [0] start, [1] after planning, [2] after the wi kernel,
- *                   [3] after the wo kernel, [4] end.
+ *   qmoe_moe_layer: [0] start, [1] after planning, [2] after the wi
+ *                   CUDA-core kernel, [3] after the wi tensor-core kernel,
+ *                   [4] after the wo CUDA-core kernel, [5] after the wo
+ *                   tensor-core kernel (and the combine when k > 1) = end.
  *   rvq_moe_layer:  [0] start, [1] after planning and the input transform,
  *                   [2] after the gate and up kernels, [3] after SwiGLU and the
  *                   down input transform, [4] after the down kernel, [5] end.
