@@ -106,7 +106,7 @@ struct SmemMap {
 };
 
 template <int NT>
-__device__ __forceinline__ void load_x(uint32_t xs, int c, uint32_t flip, uint32_t (&w)[NT / 2]) {
+__device__ __forceinline__ void load_x(uint32_t xs, int c, uint32_t (&w)[NT / 2]) {
     if constexpr (NT == 2) {
         w[0] = *(const uint32_t*)(g_smem + xs + 4u * c);
     } else if constexpr (NT == 4) {
@@ -120,9 +120,30 @@ __device__ __forceinline__ void load_x(uint32_t xs, int c, uint32_t flip, uint32
         w[2] = v.z;
         w[3] = v.w;
     }
-#pragma unroll
-    for (int q = 0; q < NT / 2; ++q) w[q] ^= flip;
 }
+
+// Mixed-precision accumulation (sm_100+): acc + bf16 and acc + bf16 * bf16 in
+// one instruction each, the bf16 operand taken from either half of a 32-bit
+// register; the bf16 -> fp32 widening is exact, so each is one fp32 rounding.
+__device__ __forceinline__ float acc_add_lo(float acc, uint32_t w) {
+    float d;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.bf16 %0, l, %2;\n}" : "=f"(d) : "r"(w), "f"(acc));
+    return d;
+}
+__device__ __forceinline__ float acc_fma_lo(float acc, uint32_t w, uint32_t sgn) {
+    float d;
+    asm("{\n .reg .b16 l, h, s, t;\n mov.b32 {l, h}, %1;\n mov.b32 {s, t}, %3;\n fma.rn.f32.bf16 %0, l, s, %2;\n}"
+        : "=f"(d) : "r"(w), "f"(acc), "r"(sgn));
+    return d;
+}
+__device__ __forceinline__ float acc_fma_hi(float acc, uint32_t w, uint32_t sgn) {
+    float d;
+    asm("{\n .reg .b16 l, h, s, t;\n mov.b32 {l, h}, %1;\n mov.b32 {s, t}, %3;\n fma.rn.f32.bf16 %0, h, s, %2;\n}"
+        : "=f"(d) : "r"(w), "f"(acc), "r"(sgn));
+    return d;
+}
+// +1 or -1 as bf16 (low half) for a compact slot: bit 0 set = negative weight.
+__device__ __forceinline__ uint32_t slot_sign(uint32_t s) { return 0x3F80u | ((s & 1u) << 15); }
 
 template <bool DICT_SMEM>
 __device__ __forceinline__ void lookup(const GemmArgs& a, const SmemMap& sm, uint32_t code, uint32_t& ea,
@@ -136,10 +157,11 @@ __device__ __forceinline__ void lookup(const GemmArgs& a, const SmemMap& sm, uin
     }
 }
 
-// Per-token sum of one codeword's weights (at most three nonzeros, from the
-// compact slots) times the staged activations, run starting at column cj.
+// Adds one codeword's weights (at most three nonzeros, from the compact
+// slots) times the staged activations to the per-token sums; the run starts
+// at column cj.  Empty slots read nothing and add zero.
 template <int NT>
-__device__ __forceinline__ void code_dot(uint32_t ea, uint32_t eb, int cj, uint32_t xs, float (&t)[NT]) {
+__device__ __forceinline__ void code_acc(uint32_t ea, uint32_t eb, int cj, uint32_t xs, float (&acc)[NT]) {
     const uint32_t s0 = (ea >> 4) & 63u, s1 = ea >> 10, s2 = eb & 63u;
     if constexpr (NT == 1) {
         const uint32_t base = xs + 4u * (uint32_t)cj;
@@ -147,19 +169,20 @@ __device__ __forceinline__ void code_dot(uint32_t ea, uint32_t eb, int cj, uint3
         if (s0 != 63u) r0 = *(const uint16_t*)(g_smem + base + 2u * s0);
         if (s1 != 63u) r1 = *(const uint16_t*)(g_smem + base + 2u * s1);
         if (s2 != 63u) r2 = *(const uint16_t*)(g_smem + base + 2u * s2);
-        t[0] = (__uint_as_float(r1 << 16) + __uint_as_float(r2 << 16)) + __uint_as_float(r0 << 16);
+        acc[0] = acc_add_lo(acc_add_lo(acc_add_lo(acc[0], r0), r1), r2);
     } else {
         constexpr int W = NT / 2;
         uint32_t w0[W], w1[W], w2[W];
 #pragma unroll
         for (int q = 0; q < W; ++q) w0[q] = w1[q] = w2[q] = 0u;
-        if (s0 != 63u) load_x<NT>(xs, cj + (int)(s0 >> 1), (s0 & 1u) * 0x80008000u, w0);
-        if (s1 != 63u) load_x<NT>(xs, cj + (int)(s1 >> 1), (s1 & 1u) * 0x80008000u, w1);
-        if (s2 != 63u) load_x<NT>(xs, cj + (int)(s2 >> 1), (s2 & 1u) * 0x80008000u, w2);
+        if (s0 != 63u) load_x<NT>(xs, cj + (int)(s0 >> 1), w0);
+        if (s1 != 63u) load_x<NT>(xs, cj + (int)(s1 >> 1), w1);
+        if (s2 != 63u) load_x<NT>(xs, cj + (int)(s2 >> 1), w2);
+        const uint32_t g0 = slot_sign(s0), g1 = slot_sign(s1), g2 = slot_sign(s2);
 #pragma unroll
         for (int q = 0; q < W; ++q) {
-            t[2 * q] = (bf16_lo(w1[q]) + bf16_lo(w2[q])) + bf16_lo(w0[q]);
-            t[2 * q + 1] = (bf16_hi(w1[q]) + bf16_hi(w2[q])) + bf16_hi(w0[q]);
+            acc[2 * q] = acc_fma_lo(acc_fma_lo(acc_fma_lo(acc[2 * q], w0[q], g0), w1[q], g1), w2[q], g2);
+            acc[2 * q + 1] = acc_fma_hi(acc_fma_hi(acc_fma_hi(acc[2 * q + 1], w0[q], g0), w1[q], g1), w2[q], g2);
         }
     }
 }
@@ -177,11 +200,12 @@ __device__ void escape_dot(const GemmArgs& a, uint32_t code, int len, int cj, ui
             t[0] += __uint_as_float(r << 16);
         } else {
             uint32_t w[NT / 2];
-            load_x<NT>(xs, cj + q, s == 1u ? 0x80008000u : 0u, w);
+            load_x<NT>(xs, cj + q, w);
+            const uint32_t g = s == 1u ? 0xBF80u : 0x3F80u;
 #pragma unroll
             for (int z = 0; z < NT / 2; ++z) {
-                t[2 * z] += bf16_lo(w[z]);
-                t[2 * z + 1] += bf16_hi(w[z]);
+                t[2 * z] = acc_fma_lo(t[2 * z], w[z], g);
+                t[2 * z + 1] = acc_fma_hi(t[2 * z + 1], w[z], g);
             }
         }
     }
@@ -230,6 +254,8 @@ __device__ __forceinline__ void window(const GemmArgs& a, const SmemMap& sm, uin
     const int col = (int)(start - (uint32_t)row * (uint32_t)cols);
     const int cross = cols - col;                 // prefix from which codewords start in the next row
     bad |= (col + sum > 2 * cols) | (row >= n_rows && sum > 0);
+    // total: all of the lane's codewords; lo: those that start in the first row
+    // (a prefix, since the codewords are in stream order)
     float total[NT], lo[NT];
 #pragma unroll
     for (int z = 0; z < NT; ++z) total[z] = lo[z] = 0.0f;
@@ -238,12 +264,10 @@ __device__ __forceinline__ void window(const GemmArgs& a, const SmemMap& sm, uin
     for (int j = 0; j < CPL; ++j) {
         const bool second = pre >= cross;
         const int cj = second ? col + pre - cols : col + pre;
-        float t[NT];
-        code_dot<NT>(ea[j], eb[j], cj, sm.xs, t);
+        code_acc<NT>(ea[j], eb[j], cj, sm.xs, total);
+        if (!second) {
 #pragma unroll
-        for (int z = 0; z < NT; ++z) {
-            total[z] += t[z];
-            if (!second) lo[z] += t[z];
+            for (int z = 0; z < NT; ++z) lo[z] = total[z];
         }
         pre += (int)(ea[j] & 15u) * 2;
     }
@@ -548,7 +572,7 @@ constexpr int kDtcThreads = 256;
 constexpr uint32_t kDtcLBO = 128, kDtcSBO = (kDtcK / 8) * 128;      // 4096 B
 constexpr int kDtcABytes = kDtcM * kDtcK * 2;                        // 64 KB
 constexpr int kDtcBBytes = kDtcN * kDtcK * 2;                        // 32 KB
-constexpr int kDtcSmem = 1024 + kDtcABytes + kDtcBBytes + 64;
+constexpr int kDtcSmem = 1024 + kDtcABytes + kDtcBBytes + 64 + 4 * kDtcN;
 constexpr uint32_t kDtcIdesc = qmoe_tc::idesc_f16(kDtcM, kDtcN, true, true);
 constexpr uint32_t kDtcSpin = 1u << 20;
 constexpr uint16_t kBf16One = 0x3F80, kBf16MinusOne = 0xBF80;
@@ -634,6 +658,7 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
     unsigned char* B = smem + kDtcABytes;
     uint64_t* bar = (uint64_t*)(B + kDtcBBytes);
     uint32_t* tmem_slot = (uint32_t*)(bar + 1);
+    int* sslot = (int*)(tmem_slot + 4);           // the tile's token slots, read once per tile
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const MatDev& m = a.m;
     if (tid == 0) {
@@ -652,6 +677,8 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
     for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
         const Job job = a.jobs[tile / a.row_tiles];
         const int r0 = (tile % a.row_tiles) * kDtcM;
+        if (tid < kDtcN) sslot[tid] = tid < job.n_tok ? a.slots[job.slot_begin + tid] : 0;
+        __syncthreads();
         const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
         const uint16_t* codes = m.codes + (m.code_base ? m.code_base[job.matrix] : 0ull);
         for (int b = 0; b < m.nb; ++b) {
@@ -671,7 +698,7 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
                     const int n = q / (kDtcK / 8), c8 = q % (kDtcK / 8);
                     const bool live = n < job.n_tok && c8 * 8 < blen;
                     const uint16_t* src = a.x;
-                    if (live) src = a.x + (size_t)(a.slots[job.slot_begin + n] / a.x_div) * m.cols + b * kDtcK + c8 * 8;
+                    if (live) src = a.x + (size_t)(sslot[n] / a.x_div) * m.cols + b * kDtcK + c8 * 8;
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
                                      smem_u32(B + (n >> 3) * kDtcSBO + c8 * kDtcLBO + (n & 7) * 16)),
                                  "l"(src), "r"(live ? 16 : 0)
@@ -712,7 +739,7 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
 #pragma unroll
                     for (int n = 0; n < 32; ++n) {
                         const int nn = 32 * half + n;
-                        if (nn < job.n_tok) store_out(a, a.slots[job.slot_begin + nn], row, s * __uint_as_float(r[n]));
+                        if (nn < job.n_tok) store_out(a, sslot[nn], row, s * __uint_as_float(r[n]));
                     }
                 }
             }

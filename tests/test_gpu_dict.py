@@ -197,7 +197,11 @@ def _layer(E, d, f, p0, seed):
 @pytest.mark.parametrize("E,d,f,T,k,p0", [(8, 256, 512, 40, 1, 0.857), (6, 128, 384, 33, 2, 0.886),
                                            (16, 768, 768, 200, 1, 0.87), (4, 256, 256, 3, 1, 0.886),
                                            # experts with >= 32 tokens take the tensor-core kernel:
-                                           (4, 776, 1040, 300, 1, 0.857), (6, 520, 264, 160, 2, 0.886)])
+                                           (4, 776, 1040, 300, 1, 0.857), (6, 520, 264, 160, 2, 0.886),
+                                           # ~75 tensor-core jobs: 4-tile (wi) and 2-tile (wo) work items
+                                           (2, 512, 1024, 4700, 1, 0.886),
+                                           # 3-tile (wi) work items, entries with more than three nonzeros
+                                           (2, 384, 768, 4700, 1, 0.857)])
 def test_moe_layer_parity(dev, E, d, f, T, k, p0):
     dd = Q.Dictionary(dictionary(p0))
     mwi, mwo, Wi, Wo = _layer(E, d, f, p0, seed=21)
