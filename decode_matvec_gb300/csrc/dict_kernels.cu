@@ -510,7 +510,9 @@ __device__ void run_tile(const GemmArgs& a, const SmemMap& sm, const Job& job, i
     __syncthreads();
 }
 
-template <bool DICT_SMEM>
+// NTMAX: the largest token class of the launch (its chunk size); a kernel
+// compiled for fewer classes needs fewer registers.
+template <bool DICT_SMEM, int NTMAX>
 __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
     const int tid = threadIdx.x, nthreads = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
@@ -545,11 +547,18 @@ __global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
         const int j = tile / a.row_tiles;
         const bool restage = j != staged;
         staged = j;
-        switch (nt_class(job.n_tok)) {
-            case 1: run_tile<1, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
-            case 2: run_tile<2, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
-            case 4: run_tile<4, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
-            default: run_tile<8, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage); break;
+        const int c = nt_class(job.n_tok);
+        if (c == 1 || NTMAX == 1) {
+            run_tile<1, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage);
+        } else if (c == 2 || NTMAX == 2) {
+            if constexpr (NTMAX >= 2)
+                run_tile<2, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage);
+        } else if (c == 4 || NTMAX == 4) {
+            if constexpr (NTMAX >= 4)
+                run_tile<4, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage);
+        } else {
+            if constexpr (NTMAX >= 8)
+                run_tile<8, DICT_SMEM>(a, sm, job, r0, r1, tid, nthreads, warp, nwarps, lane, tile + 2, t_end, restage);
         }
     }
 }
@@ -1038,6 +1047,16 @@ MatDev to_dev(const qmoe_matrix_set* s) {
     return m;
 }
 
+template <bool DICT_SMEM, int NTMAX>
+int launch_gemm_as(const GemmArgs& a, unsigned grid, int threads, size_t smem, cudaStream_t st) {
+    int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<DICT_SMEM, NTMAX>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
+                              "cudaFuncSetAttribute");
+    if (rc) return rc;
+    dict_gemm_kernel<DICT_SMEM, NTMAX><<<grid, threads, smem, st>>>(a);
+    return QMOE_OK;
+}
+
 int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaStream_t st, long long tiles_hint) {
     const int sms = qmoe::sm_count();
     a.nt_max = nt_max;
@@ -1047,20 +1066,21 @@ int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaS
     a.inv_cols = 1.0f / (float)a.m.cols;
     const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + tile_smem(a.m.cols, nt_max);
     if (smem > (size_t)kSmemMax) return qmoe::fail(QMOE_EUNSUPPORTED, "dict_gemm: tile does not fit in shared memory");
-    if (dict_smem) {
-        int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<true>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
-                                  "cudaFuncSetAttribute");
-        if (rc) return rc;
-        dict_gemm_kernel<true><<<sms, kThreadsSmemDict, smem, st>>>(a);
-    } else {
-        int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<false>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
-                                  "cudaFuncSetAttribute");
-        if (rc) return rc;
-        const long long grid = std::max(1LL, std::min(tiles_hint, (long long)sms * 4));
-        dict_gemm_kernel<false><<<(unsigned)grid, kThreadsGlobalDict, smem, st>>>(a);
+    const unsigned grid = dict_smem ? (unsigned)sms : (unsigned)std::max(1LL, std::min(tiles_hint, (long long)sms * 4));
+    const int threads = dict_smem ? kThreadsSmemDict : kThreadsGlobalDict;
+    int rc;
+    switch ((dict_smem ? 16 : 0) + nt_max) {
+        case 16 + 1: rc = launch_gemm_as<true, 1>(a, grid, threads, smem, st); break;
+        case 16 + 2: rc = launch_gemm_as<true, 2>(a, grid, threads, smem, st); break;
+        case 16 + 4: rc = launch_gemm_as<true, 4>(a, grid, threads, smem, st); break;
+        case 16 + 8: rc = launch_gemm_as<true, 8>(a, grid, threads, smem, st); break;
+        case 1: rc = launch_gemm_as<false, 1>(a, grid, threads, smem, st); break;
+        case 2: rc = launch_gemm_as<false, 2>(a, grid, threads, smem, st); break;
+        case 4: rc = launch_gemm_as<false, 4>(a, grid, threads, smem, st); break;
+        case 8: rc = launch_gemm_as<false, 8>(a, grid, threads, smem, st); break;
+        default: return qmoe::fail(QMOE_EINVAL, "dict_gemm: token chunk must be 1, 2, 4 or 8");
     }
+    if (rc) return rc;
     return qmoe::launch_check("dict_gemm_kernel");
 }
 
