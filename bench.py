@@ -466,6 +466,33 @@ def extra_rows(layer, device, peak):
                         "us_per_call": t * 1e6, "stream_bytes": sb})
         return out
     guarded(linear)
+
+    def device_encoder():
+        # qmoe_pack_device on c2048-shaped wi matrices (6144 x 2080), against the host encoder
+        cfg = CFG
+        lib = native_synth()
+        rows_, cols_ = synth.dict_matrix_shape(cfg, synth.WI)
+        tern = np.empty((rows_, cols_), np.int8)
+        lib.synth_ternary_rows(cfg.seed, 0, synth.WI, cols_, synth.zero_threshold(cfg.p0), 0, rows_, tern.ctypes.data)
+        words = layer.words
+        t0 = time.perf_counter()
+        hc, ho = Q.qmoe_pack(tern, words)
+        host_s = time.perf_counter() - t0
+        tt = torch.from_numpy(tern).to(device)
+        codes = torch.zeros(rows_ * cols_ // 2, dtype=torch.int16, device=device)
+        off = torch.zeros(ho.size, dtype=torch.int32, device=device)
+        ws = torch.empty(Q.qmoe_pack_device_ws_size(rows_, cols_), dtype=torch.uint8, device=device)
+        t = _time_calls(lambda: Q.qmoe_pack_device(layer.dictionary, tt, codes, off, ws), n=20, warm=3)
+        same = (Q.qmoe_check_status() == Q.QMOE_OK and
+                np.array_equal(off.cpu().numpy().view(np.uint32), ho) and
+                np.array_equal(codes[:hc.size].cpu().numpy().view(np.uint16), hc))
+        w = rows_ * cols_
+        return {"workload": f"device encoder qmoe_pack_device, {cfg.name} wi matrix {rows_}x{cols_} "
+                            f"(p0={cfg.p0}, 256-weight blocks)",
+                "weights_per_s": w / t, "ms_per_matrix": t * 1e3,
+                "host_encoder_weights_per_s": w / host_s, "host_encoder_threads": 1,
+                "equal_to_host_encoder": bool(same)}
+    guarded(device_encoder)
     return rows
 
 

@@ -32,7 +32,7 @@ EXPORTED = [
     "qmoe_bucketise", "qmoe_moe_layer_ws_size", "qmoe_moe_layer", "rvq_expert_matmul_ws_size",
     "rvq_expert_matmul", "rvq_moe_layer_ws_size", "rvq_moe_layer", "rvq_pack", "qmoe_check_status",
     "qmoe_last_error", "qmoe_decode_dense", "rvq_decode_dense", "qmoe_set_phase_events",
-    "qmoe_moe_layer_noalloc",
+    "qmoe_moe_layer_noalloc", "qmoe_pack_device_ws_size", "qmoe_pack_device",
 ]
 
 
@@ -85,6 +85,8 @@ _sig = {
     "rvq_decode_dense": [_vp, _vp, _vp],
     "qmoe_set_phase_events": [_vp, _i],
     "qmoe_moe_layer_noalloc": [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _vp],
+    "qmoe_pack_device_ws_size": [_i, _i, _i, _vp],
+    "qmoe_pack_device": [_vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp, _sz, _vp],
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -263,6 +265,23 @@ def qmoe_bucketise(ids, E: int, counts, offsets, perm, stream=None):
     T, k = ids.shape
     _check(_lib.qmoe_bucketise(_dptr(ids), T, k, E, _dptr(counts), _dptr(offsets), _dptr(perm), _stream_ptr(stream)),
            "qmoe_bucketise")
+
+
+def qmoe_pack_device_ws_size(rows: int, cols: int, block: int = 256) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.qmoe_pack_device_ws_size(rows, cols, block, ctypes.byref(n)), "qmoe_pack_device_ws_size")
+    return n.value
+
+
+def qmoe_pack_device(d: Dictionary, tern, codes, blk_off, workspace, block: int = 256, stream=None):
+    """Device encoder: codewords and block offsets of the int8 ternary matrix `tern` (device tensor
+    [rows, cols]) into `codes` (int16-viewed uint16) and `blk_off` (int32-viewed uint32, rows*nb + 1).
+    The codeword count is blk_off[-1] once the stream has reached the end of the call."""
+    rows, cols = tern.shape
+    _check(_lib.qmoe_pack_device(ctypes.byref(d.c), _dptr(tern), rows, cols, block, _dptr(codes),
+                                 int(codes.numel()), _dptr(blk_off), _dptr(workspace), int(workspace.numel()),
+                                 _stream_ptr(stream)), "qmoe_pack_device")
+    return codes, blk_off
 
 
 def qmoe_moe_layer_ws_size(E, d_model, d_ff, T, k) -> int:

@@ -30,6 +30,7 @@ inline int launch_check(const char* where) { return cuda_check(cudaGetLastError(
 // that reads and clears it (synchronously, after the caller synchronised).
 int dict_take_error();
 int rvq_take_error();
+int pack_take_error();
 
 // Unit of work of the expert kernels: one expert matrix applied to up to
 // `n_tok` tokens whose slots are slots[slot_begin .. slot_begin + n_tok).

@@ -1335,9 +1335,12 @@ extern "C" int qmoe_check_status(void* stream) {
     if (e != cudaSuccess) return qmoe::cuda_check(e, "qmoe_check_status");
     const int a = qmoe::dict_take_error();
     const int b = qmoe::rvq_take_error();
-    if (a == QMOE_ECUDA || b == QMOE_ECUDA) return fail(QMOE_ECUDA, "qmoe_check_status: reading the error word failed");
+    const int c = qmoe::pack_take_error();
+    if (a == QMOE_ECUDA || b == QMOE_ECUDA || c == QMOE_ECUDA)
+        return fail(QMOE_ECUDA, "qmoe_check_status: reading the error word failed");
     if (a) return fail(a, "device reported an error (dictionary kernels)");
     if (b) return fail(b, "device reported an error (RVQ kernels)");
+    if (c) return fail(c, "device reported an error (device encoder)");
     return QMOE_OK;
 }
 

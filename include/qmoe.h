@@ -140,6 +140,37 @@ typedef struct {
 } qmoe_dict;
 
 /*
+ * Device encoder: the greedy longest-match encoding of qmoe_pack on the GPU,
+ * with the same codewords and block offsets bit for bit (QMoE page,
+ * "Encoding (compression time)"; the page encodes on the host, one thread per
+ * row).  One GPU thread encodes one (row, block) against a hash table of the
+ * dictionary that the call builds in the workspace; a scan of the per-block
+ * counts gives the offsets.  Asynchronous on `stream`.
+ *
+ *  dict      device descriptor; only dict->words is read.
+ *  tern      device int8 [rows][cols] in {-1,0,+1}.
+ *  rows >= 0; cols, block even, > 0.
+ *  codes     device out uint16 [codes_cap].  rows*cols/2 codewords always
+ *            suffice; the exact count is blk_off[rows*nb] once the stream has
+ *            reached the end of the call.
+ *  blk_off   device out uint32 [rows*nb + 1], nb = ceil(cols/block): the
+ *            qmoe_pack layout.
+ *  workspace device scratch of qmoe_pack_device_ws_size() bytes (a 3 MB
+ *            dictionary table plus rows*nb*block bytes); caller-owned, not
+ *            shared by concurrent calls.
+ * Errors on the host: EINVAL (shape, NULL), ECAPACITY (workspace too small),
+ * ECUDA.  Errors found on the device go to the error word that
+ * qmoe_check_status() returns: EINVAL (a weight outside {-1,0,1}, more than
+ * 2^32 codewords), EFORMAT (bad dictionary entry, or a block the dictionary
+ * cannot express), ECAPACITY (more codewords than codes_cap: the excess is
+ * dropped).
+ */
+int qmoe_pack_device_ws_size(int rows, int cols, int block, size_t* bytes);
+int qmoe_pack_device(const qmoe_dict* dict, const int8_t* tern, int rows, int cols, int block,
+                     uint16_t* codes, size_t codes_cap, uint32_t* blk_off, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/*
  * `count` dictionary-coded matrices of the same shape (e.g. the wi matrices
  * of all experts of a layer).  Matrix e's codewords start at
  * codes[code_base[e]]; its block offsets are blk_off[e*(rows*nb+1) + ...],
@@ -345,8 +376,9 @@ int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_out,
  */
 int qmoe_set_phase_events(void* const* events, int n);
 
-/* Synchronises `stream`, returns and clears the device error word
- * (QMOE_OK, QMOE_EFORMAT, QMOE_EINVAL or QMOE_ETIMEOUT), or QMOE_ECUDA. */
+/* Synchronises `stream`, returns and clears the device error words
+ * (QMOE_OK, QMOE_EFORMAT, QMOE_EINVAL, QMOE_ECAPACITY or QMOE_ETIMEOUT), or
+ * QMOE_ECUDA. */
 int qmoe_check_status(void* stream);
 
 /* Message describing the calling thread's last failed call ("" if none). */
