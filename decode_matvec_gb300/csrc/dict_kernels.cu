@@ -41,7 +41,28 @@ constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + 
 constexpr int kBudgetGlobalDict = 56 * 1024;                    // activations + row sums, dictionary via L1/L2
 constexpr int kSaccBytes = 8192;                                // per-tile row sums (rows x tokens x 4 B)
 constexpr int kTcMinTokens = 32;                                // experts this busy use the tensor-core kernel
-constexpr int kThreadsSmemDict = 512;
+// Threads of a block with the dictionary in SMEM, by the launch's largest
+// token class: fewer accumulators per thread leave registers for more warps,
+// which hide more of the shared-memory gather latency (measured on the
+// c2048-shaped layer: 512 threads for every class 6.69 ms per T=4096 step,
+// 640 / 768 threads for the 4- / 2-token classes 6.33 ms).
+#ifndef QMOE_THREADS_NT1
+#define QMOE_THREADS_NT1 512
+#endif
+#ifndef QMOE_THREADS_NT2
+#define QMOE_THREADS_NT2 768
+#endif
+#ifndef QMOE_THREADS_NT4
+#define QMOE_THREADS_NT4 640
+#endif
+__host__ __device__ constexpr int threads_smem_dict(int nt_max) {
+    return nt_max == 1 ? QMOE_THREADS_NT1 : nt_max == 2 ? QMOE_THREADS_NT2 : nt_max == 4 ? QMOE_THREADS_NT4 : 512;
+}
+template <bool DICT_SMEM, int NTMAX>
+struct GemmBounds {
+    static constexpr int threads = DICT_SMEM ? threads_smem_dict(NTMAX) : 256;
+    static constexpr int blocks = DICT_SMEM ? 1 : 2;
+};
 constexpr int kThreadsGlobalDict = 256;
 
 struct MatDev {
@@ -513,7 +534,8 @@ __device__ void run_tile(const GemmArgs& a, const SmemMap& sm, const Job& job, i
 // NTMAX: the largest token class of the launch (its chunk size); a kernel
 // compiled for fewer classes needs fewer registers.
 template <bool DICT_SMEM, int NTMAX>
-__global__ void __launch_bounds__(512, 1) dict_gemm_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(GemmBounds<DICT_SMEM, NTMAX>::threads, GemmBounds<DICT_SMEM, NTMAX>::blocks)
+    dict_gemm_kernel(const GemmArgs a) {
     const int tid = threadIdx.x, nthreads = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
     SmemMap sm;
@@ -1067,7 +1089,7 @@ int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaS
     const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + tile_smem(a.m.cols, nt_max);
     if (smem > (size_t)kSmemMax) return qmoe::fail(QMOE_EUNSUPPORTED, "dict_gemm: tile does not fit in shared memory");
     const unsigned grid = dict_smem ? (unsigned)sms : (unsigned)std::max(1LL, std::min(tiles_hint, (long long)sms * 4));
-    const int threads = dict_smem ? kThreadsSmemDict : kThreadsGlobalDict;
+    const int threads = dict_smem ? threads_smem_dict(nt_max) : kThreadsGlobalDict;
     int rc;
     switch ((dict_smem ? 16 : 0) + nt_max) {
         case 16 + 1: rc = launch_gemm_as<true, 1>(a, grid, threads, smem, st); break;
@@ -1252,10 +1274,11 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     const bool big = slots >= 16;
     const int budget = big ? kBudgetSmemDict : kBudgetGlobalDict;
     const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
-    const int nw = (big ? kThreadsSmemDict : kThreadsGlobalDict) / 32;
+    const int nw_wi = (big ? threads_smem_dict(nt_wi) : kThreadsGlobalDict) / 32;
+    const int nw_wo = (big ? threads_smem_dict(nt_wo) : kThreadsGlobalDict) / 32;
     const long long min_tiles = big ? 0 : 2LL * qmoe::sm_count();
-    const int rpt_wi = nt_wi ? rows_per_tile_for(d_ff, nt_wi, nw, slots, min_tiles) : 0;
-    const int rpt_wo = nt_wo ? rows_per_tile_for(d_model, nt_wo, nw, slots, min_tiles) : 0;
+    const int rpt_wi = nt_wi ? rows_per_tile_for(d_ff, nt_wi, nw_wi, slots, min_tiles) : 0;
+    const int rpt_wo = nt_wo ? rows_per_tile_for(d_model, nt_wo, nw_wo, slots, min_tiles) : 0;
     if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
     cudaStream_t st = (cudaStream_t)stream;
     // experts with at least kTcMinTokens tokens take the tensor-core kernel
