@@ -39,7 +39,10 @@ constexpr int kSlotEmpty = 63;
 constexpr int kSmemMax = 232448;                        // 227 KB opt-in per block
 constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + row sums, dictionary in SMEM
 constexpr int kBudgetGlobalDict = 56 * 1024;                    // activations + row sums, dictionary via L1/L2
-constexpr int kSaccBytes = 8192;                                // per-tile row sums (rows x tokens x 4 B)
+constexpr int kSaccBytes = 8192;                                // per-tile row sums (rows x tokens x 4 B), at least
+#ifndef QMOE_SACC_MAX
+#define QMOE_SACC_MAX 16384                                     // ... and at most, where the SMEM budget allows
+#endif
 constexpr int kTcMinTokens = 32;                                // experts this busy use the tensor-core kernel
 // Threads of a block with the dictionary in SMEM, by the launch's largest
 // token class: fewer accumulators per thread leave registers for more warps,
@@ -1036,18 +1039,26 @@ int nt_max_for(int cols, int budget) {
     return 0;
 }
 
+// Row-sum bytes of a tile: the SMEM the staged activations leave, within
+// [kSaccBytes, QMOE_SACC_MAX].
+int sacc_bytes_for(int cols, int nt, int budget) {
+    const long long left = (long long)budget - (long long)xs_bytes(cols, nt);
+    return (int)std::max<long long>(kSaccBytes, std::min<long long>(QMOE_SACC_MAX, left) & ~15LL);
+}
+
 // Rows per tile: as many as the row-sum buffer holds for nt tokens, split evenly,
 // a multiple of the warp count; at least `min_tiles` tiles when given.
-int rows_per_tile_for(int rows, int nt, int nwarps, long long n_jobs, long long min_tiles) {
-    int cap = kSaccBytes / (4 * nt);
+int rows_per_tile_for(int rows, int nt, int nwarps, long long n_jobs, long long min_tiles, int sacc_bytes) {
+    int cap = sacc_bytes / (4 * nt);
     if (min_tiles > 0) {
         const long long per_job = (min_tiles + std::max(1LL, n_jobs) - 1) / std::max(1LL, n_jobs);
         cap = (int)std::max<long long>(nwarps, std::min<long long>(cap, (rows + per_job - 1) / per_job));
     }
-    const int n = (rows + cap - 1) / cap;
-    int rpt = (rows + n - 1) / n;
-    rpt = (rpt + nwarps - 1) / nwarps * nwarps;
-    return std::min(rpt, cap / nwarps * nwarps > 0 ? cap / nwarps * nwarps : nwarps);
+    // the cap in whole warps, then tiles as equal as whole warps allow
+    const int cap_w = std::max(nwarps, cap / nwarps * nwarps);
+    const int n = (rows + cap_w - 1) / cap_w;
+    const int rpt = ((rows + n - 1) / n + nwarps - 1) / nwarps * nwarps;
+    return std::min(rpt, cap_w);
 }
 
 bool valid_set(const qmoe_matrix_set* s) {
@@ -1086,7 +1097,8 @@ int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaS
     a.row_tiles = (a.m.rows + rows_per_tile - 1) / rows_per_tile;
     a.xs_bytes = (int)xs_bytes(a.m.cols, nt_max);
     a.inv_cols = 1.0f / (float)a.m.cols;
-    const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + tile_smem(a.m.cols, nt_max);
+    const size_t smem = (dict_smem ? (size_t)kDictBytes : 0) + xs_bytes(a.m.cols, nt_max) +
+                        std::max<size_t>(kSaccBytes, ((size_t)rows_per_tile * nt_max * 4 + 15) & ~(size_t)15);
     if (smem > (size_t)kSmemMax) return qmoe::fail(QMOE_EUNSUPPORTED, "dict_gemm: tile does not fit in shared memory");
     const unsigned grid = dict_smem ? (unsigned)sms : (unsigned)std::max(1LL, std::min(tiles_hint, (long long)sms * 4));
     const int threads = dict_smem ? threads_smem_dict(nt_max) : kThreadsGlobalDict;
@@ -1184,7 +1196,8 @@ extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* 
     a.y_is_f32 = y_is_f32 ? 1 : 0;
     a.out = y;
     const long long jobs = (T + nt_max - 1) / nt_max;
-    const int rpt = rows_per_tile_for(mat->rows, nt_max, kThreadsGlobalDict / 32, jobs, 2LL * qmoe::sm_count());
+    const int rpt = rows_per_tile_for(mat->rows, nt_max, kThreadsGlobalDict / 32, jobs, 2LL * qmoe::sm_count(),
+                                      kSaccBytes);
     return launch_gemm(a, false, nt_max, rpt, (cudaStream_t)stream, jobs * ((mat->rows + rpt - 1) / rpt));
 }
 
@@ -1276,9 +1289,14 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
     const int nw_wi = (big ? threads_smem_dict(nt_wi) : kThreadsGlobalDict) / 32;
     const int nw_wo = (big ? threads_smem_dict(nt_wo) : kThreadsGlobalDict) / 32;
-    const long long min_tiles = big ? 0 : 2LL * qmoe::sm_count();
-    const int rpt_wi = nt_wi ? rows_per_tile_for(d_ff, nt_wi, nw_wi, slots, min_tiles) : 0;
-    const int rpt_wo = nt_wo ? rows_per_tile_for(d_model, nt_wo, nw_wo, slots, min_tiles) : 0;
+#ifndef QMOE_MIN_TILES_PER_SM
+#define QMOE_MIN_TILES_PER_SM 2
+#endif
+    const long long min_tiles = (long long)QMOE_MIN_TILES_PER_SM * qmoe::sm_count();
+    const int rpt_wi = nt_wi ? rows_per_tile_for(d_ff, nt_wi, nw_wi, slots, min_tiles,
+                                                 big ? sacc_bytes_for(d_model, nt_wi, budget) : kSaccBytes) : 0;
+    const int rpt_wo = nt_wo ? rows_per_tile_for(d_model, nt_wo, nw_wo, slots, min_tiles,
+                                                 big ? sacc_bytes_for(d_ff, nt_wo, budget) : kSaccBytes) : 0;
     if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
     cudaStream_t st = (cudaStream_t)stream;
     // experts with at least kTcMinTokens tokens take the tensor-core kernel
