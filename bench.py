@@ -493,7 +493,63 @@ def extra_rows(layer, device, peak):
                 "host_encoder_weights_per_s": w / host_s, "host_encoder_threads": 1,
                 "equal_to_host_encoder": bool(same)}
     guarded(device_encoder)
+    guarded(lambda: _dense_baseline_row(layer, device))
     return rows
+
+
+def _dense_baseline_row(layer, device):
+    """The same layer step with uncompressed bf16 weights: per touched expert, cuBLAS GEMMs
+    h = relu(x_e Wi_e^T), o = h Wo_e^T, gated scatter into y; replayed from a CUDA graph so that
+    launch overhead is not timed.  The dense weights are fresh ternary draws with the layer's p0 and
+    shapes (their values do not change the time), only for the experts this batch touches."""
+    import torch
+    cfg = CFG
+    st = DictStep(layer, cfg, T_MAIN, 0, device)
+    st.run()
+    ids = st.ids.view(-1)
+    x = st.x.view(torch.bfloat16)
+    gates = st.gates.view(-1)
+    touched = torch.unique(ids).tolist()
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg.seed)
+
+    def ternary(rows, cols):
+        u = torch.rand((rows, cols), generator=g, device=device)
+        w = torch.where(u < cfg.p0, 0.0, torch.where(u < (1 + cfg.p0) / 2, -1.0, 1.0))
+        return w.to(torch.bfloat16)
+
+    experts = []
+    for e in touched:
+        idx = torch.nonzero(ids == e).view(-1)
+        experts.append((idx, ternary(cfg.d_ff, cfg.d_model), ternary(cfg.d_model, cfg.d_ff)))
+    y = torch.zeros((T_MAIN, cfg.d_model), dtype=torch.float32, device=device)
+
+    def step():
+        y.zero_()
+        for idx, wi, wo in experts:
+            xe = x.index_select(0, idx)
+            h = torch.relu(xe @ wi.t())
+            o = (h @ wo.t()).float() * gates.index_select(0, idx).unsqueeze(1)
+            y.index_add_(0, idx, o)
+
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    t = _time_calls(graph.replay, n=20, warm=3)
+    dense_bytes = len(experts) * 2 * cfg.d_ff * cfg.d_model * 2
+    del experts, graph
+    torch.cuda.empty_cache()
+    return {"workload": f"dense bf16 baseline: {cfg.name} layer step with uncompressed weights, T={T_MAIN} "
+                        f"(cuBLAS per-expert GEMMs, CUDA graph)",
+            "tokens_per_s": T_MAIN / t, "ms_per_step": t * 1e3, "touched_experts": len(touched),
+            "dense_weight_bytes": dense_bytes, "dense_weight_gbs": dense_bytes / t / 1e9,
+            "dense_ms_at_hbm_peak": dense_bytes / (hbm_peak()[0] * 1e9) * 1e3}
 
 
 # ---------------------------------------------------------------- main
