@@ -633,27 +633,37 @@ __device__ __forceinline__ void store_out(const GemmArgs& a, int slot, int row, 
     }
 }
 
-// One thread expands the codewords of (row, block) into its row of the tile.
-// The codewords are read 16 at a time, then all their dictionary entries, so
-// that a block costs a few memory round trips instead of two per codeword.
-__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, uint32_t lo, uint32_t hi,
+// Component q (0..3, a constant after unrolling) of a uint4.
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
+
+// One thread expands the codewords [lo, hi) (absolute indices into `codes`)
+// of (row, block) into its row of the tile.  Codewords are read 16 at a time
+// as aligned 16-byte chunks, then all their compact entries, so that a block
+// costs a few memory round trips instead of two per codeword.
+__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, uint64_t lo, uint64_t hi,
                                                  int blen, unsigned char* A, int rl, bool& bad) {
-    constexpr int CH = 16;
     unsigned char* rowbase = A + (rl >> 3) * kDtcSBO + (rl & 7) * 16;
+    if (hi < lo || hi - lo > (uint64_t)(blen / 2)) {         // every codeword covers at least two weights
+        bad = true;
+        return;
+    }
     int col = 0;
-    for (uint32_t i0 = lo; i0 < hi; i0 += CH) {
-        uint32_t code[CH], ea[CH], eb[CH];
+    for (uint64_t c8 = lo & ~7ull; c8 < hi; c8 += 16) {
+        const uint4 ch0 = __ldg((const uint4*)(codes + c8));
+        const uint4 ch1 = c8 + 8 < hi ? __ldg((const uint4*)(codes + c8 + 8)) : make_uint4(0, 0, 0, 0);
+        uint32_t code[16], ea[16], eb[16];
 #pragma unroll
-        for (int k = 0; k < CH; ++k) code[k] = i0 + k < hi ? (uint32_t)__ldg(codes + i0 + k) : 0u;
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-            ea[k] = i0 + k < hi ? (uint32_t)__ldg(a.dictA + code[k]) : 0u;
-            eb[k] = i0 + k < hi ? (uint32_t)__ldg(a.dictB + code[k]) : 63u;
+        for (int k = 0; k < 16; ++k) {
+            const uint32_t w = u4_at(k < 8 ? ch0 : ch1, (k >> 1) & 3);
+            code[k] = (w >> (16 * (k & 1))) & 0xFFFFu;
+            const bool in = c8 + k >= lo && c8 + k < hi;
+            ea[k] = in ? (uint32_t)__ldg(a.dictA + code[k]) : 0u;
+            eb[k] = in ? (uint32_t)__ldg(a.dictB + code[k]) : 63u;
         }
 #pragma unroll
-        for (int k = 0; k < CH; ++k) {
+        for (int k = 0; k < 16; ++k) {
             const int len = (int)(ea[k] & 15u) * 2;
-            if (len == 0) continue;
+            if (len == 0) continue;                       // outside [lo, hi): every entry has a pair
             if (col + len > blen) {
                 bad = true;
                 break;
@@ -714,7 +724,7 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
         if (tid < kDtcN) sslot[tid] = tid < job.n_tok ? a.slots[job.slot_begin + tid] : 0;
         __syncthreads();
         const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
-        const uint16_t* codes = m.codes + (m.code_base ? m.code_base[job.matrix] : 0ull);
+        const uint64_t cbase = m.code_base ? m.code_base[job.matrix] : 0ull;
         for (int b = 0; b < m.nb; ++b) {
             const int blen = min(kDtcK, m.cols - b * kDtcK);
             // zero the weight tile (16 bytes per store)
@@ -723,8 +733,8 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
             if (tid < kDtcM) {
                 const int row = r0 + tid;
                 if (row < m.rows)
-                    decode_row_block(a, codes, off[(size_t)row * m.nb + b], off[(size_t)row * m.nb + b + 1], blen, A,
-                                     tid, bad);
+                    decode_row_block(a, m.codes, cbase + off[(size_t)row * m.nb + b],
+                                     cbase + off[(size_t)row * m.nb + b + 1], blen, A, tid, bad);
             } else {
                 // activations: 64 tokens x 256 columns in 16-byte asynchronous copies
                 // (zero-filled past the tokens and columns that exist), all in flight at once
