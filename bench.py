@@ -494,7 +494,64 @@ def extra_rows(layer, device, peak):
                 "equal_to_host_encoder": bool(same)}
     guarded(device_encoder)
     guarded(lambda: _dense_baseline_row(layer, device))
+    guarded(lambda: _materialise_row(layer, device, 64))
     return rows
+
+
+def _expert_view(Q, ms, host, e):
+    """A count-1 matrix descriptor for expert e of a device matrix set."""
+    import ctypes
+    nb = (ms.cols + ms.block - 1) // ms.block
+    base = int(host.code_base[e])
+    c = Q.CMatrixSet(ms.codes.data_ptr() + 2 * base, None, ms.blk_off.data_ptr() + 4 * e * (ms.rows * nb + 1),
+                     ms.scale.data_ptr() + 2 * e * ms.rows, 1, ms.rows, ms.cols, ms.block)
+    view = type("ExpertView", (), {})()
+    view.c = c
+    return view
+
+
+def _materialise_row(layer, device, T):
+    """The unfused alternative: decode each touched expert's wi and wo to dense fp32 in HBM
+    (qmoe_decode_dense), then cuBLAS GEMMs; replayed from a CUDA graph."""
+    import torch
+    import decode_matvec_gb300 as Q
+    cfg = CFG
+    st = DictStep(layer, cfg, T, 0, device)
+    st.run()
+    ids = st.ids.view(-1)
+    x = st.x.view(torch.bfloat16).float()
+    gates = st.gates.view(-1)
+    touched = torch.unique(ids).tolist()
+    wi_d = torch.empty((cfg.d_ff, cfg.d_model), dtype=torch.float32, device=device)
+    wo_d = torch.empty((cfg.d_model, cfg.d_ff), dtype=torch.float32, device=device)
+    plan = [(torch.nonzero(ids == e).view(-1), _expert_view(Q, layer.wi, layer.wi_host, e),
+             _expert_view(Q, layer.wo, layer.wo_host, e)) for e in touched]
+    y = torch.zeros((T, cfg.d_model), dtype=torch.float32, device=device)
+
+    def step():
+        y.zero_()
+        for idx, vi, vo in plan:
+            Q.qmoe_decode_dense(layer.dictionary, vi, wi_d)
+            h = torch.relu(x.index_select(0, idx) @ wi_d.t()).to(torch.bfloat16).float()
+            Q.qmoe_decode_dense(layer.dictionary, vo, wo_d)
+            y.index_add_(0, idx, (h @ wo_d.t()) * gates.index_select(0, idx).unsqueeze(1))
+
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    t = _time_calls(graph.replay, n=20, warm=3)
+    ok = Q.qmoe_check_status() == Q.QMOE_OK
+    fused = _time_calls(st.run, n=50, warm=5)
+    return {"workload": f"materialise-then-GEMM baseline: {cfg.name} layer, T={T} (qmoe_decode_dense to fp32 in HBM "
+                        f"per touched expert, then cuBLAS; CUDA graph)",
+            "tokens_per_s": T / t, "ms_per_step": t * 1e3, "touched_experts": len(touched),
+            "fused_ms_per_step": fused * 1e3, "status_ok": ok}
 
 
 def _dense_baseline_row(layer, device):
