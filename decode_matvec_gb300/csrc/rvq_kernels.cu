@@ -63,6 +63,25 @@ __device__ void fwht_smem(float* s, int n, float norm) {
     __syncthreads();
 }
 
+// `count` normalised Walsh-Hadamard transforms of n floats each, stored back
+// to back in shared memory, in place: every butterfly stage of all of them
+// between the same two barriers.  Every thread of the block must call it.
+__device__ void fwht_smem_batch(float* s, int n, int count, float norm) {
+    const int half = n >> 1, lg = 31 - __clz(half);
+    for (int h = 1; h < n; h <<= 1) {
+        for (int b = threadIdx.x; b < count * half; b += blockDim.x) {
+            const int c = b >> lg, bb = b & (half - 1);
+            const int i = c * n + (((bb & ~(h - 1)) << 1) | (bb & (h - 1)));
+            const float a = s[i], d = s[i + h];
+            s[i] = a + d;
+            s[i + h] = a - d;
+        }
+        __syncthreads();
+    }
+    for (int i = threadIdx.x; i < count * n; i += blockDim.x) s[i] *= norm;
+    __syncthreads();
+}
+
 // x'[row] = H (D_in x[src]) for one or two sign vectors (gate and up share the input).
 __global__ void in_transform_kernel(const uint16_t* __restrict__ x, int x_div, const int32_t* __restrict__ expert_of,
                                     int k_of, const int8_t* __restrict__ si0, const int8_t* __restrict__ si1, int n,
@@ -79,8 +98,7 @@ __global__ void in_transform_kernel(const uint16_t* __restrict__ x, int x_div, c
         if (si1) s1[i] = v * (float)si1[(size_t)e * n + i];
     }
     __syncthreads();
-    fwht_smem(s0, n, norm);
-    if (si1) fwht_smem(s1, n, norm);
+    fwht_smem_batch(s0, n, si1 ? 2 : 1, norm);
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         out0[(size_t)row * n + i] = s0[i];
         if (si1) out1[(size_t)row * n + i] = s1[i];
@@ -104,8 +122,7 @@ __global__ void swiglu_transform_kernel(const float* __restrict__ gp, const floa
         su[i] = up[(size_t)row * n + i];
     }
     __syncthreads();
-    fwht_smem(sg, n, norm);
-    fwht_smem(su, n, norm);
+    fwht_smem_batch(sg, n, 2, norm);
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         const float g = sg[i] * (float)so_g[(size_t)e * n + i];
         const float u = su[i] * (float)so_u[(size_t)e * n + i];
@@ -118,24 +135,32 @@ __global__ void swiglu_transform_kernel(const float* __restrict__ gp, const floa
     for (int i = threadIdx.x; i < n; i += blockDim.x) out[(size_t)row * n + i] = sg[i];
 }
 
-// y[t] = sum_j gate[t][j] * D_out H y'[t*k + j]  (k == 1 and gates == NULL: plain output transform)
+// y[t] = sum_j gate[t][j] * D_out H y'[t*k + j]  (k == 1 and gates == NULL: plain output transform).
+// The slots of a token are transformed kg at a time (kg * n floats of shared
+// memory, plus n for the sum).
 __global__ void out_transform_kernel(const float* __restrict__ yp, const int32_t* __restrict__ expert_of,
-                                     const int8_t* __restrict__ so, const float* __restrict__ gates, int k, int n,
-                                     float norm, void* __restrict__ y, int y_is_f32) {
+                                     const int8_t* __restrict__ so, const float* __restrict__ gates, int k, int kg,
+                                     int n, float norm, void* __restrict__ y, int y_is_f32) {
     extern __shared__ float sm[];
+    float* acc = sm + (size_t)kg * n;
     const int t = blockIdx.x;
-    float* s = sm;
-    float* acc = sm + n;
     for (int i = threadIdx.x; i < n; i += blockDim.x) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-        const int slot = t * k + j;
-        const int e = expert_of ? expert_of[slot] : 0;
-        const float g = gates ? gates[slot] : 1.0f;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) s[i] = yp[(size_t)slot * n + i];
+    for (int j0 = 0; j0 < k; j0 += kg) {
+        const int cnt = min(kg, k - j0);
+        __syncthreads();                                  // the previous group is consumed
+        for (int i = threadIdx.x; i < cnt * n; i += blockDim.x) sm[i] = yp[((size_t)t * k + j0) * n + i];
         __syncthreads();
-        fwht_smem(s, n, norm);
-        for (int i = threadIdx.x; i < n; i += blockDim.x) acc[i] = fmaf(g, s[i] * (float)so[(size_t)e * n + i], acc[i]);
-        __syncthreads();
+        fwht_smem_batch(sm, n, cnt, norm);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            float a = acc[i];
+            for (int j = 0; j < cnt; ++j) {
+                const int slot = t * k + j0 + j;
+                const int e = expert_of ? expert_of[slot] : 0;
+                const float g = gates ? gates[slot] : 1.0f;
+                a = fmaf(g, sm[(size_t)j * n + i] * (float)so[(size_t)e * n + i], a);
+            }
+            acc[i] = a;                                   // the same thread reads it back
+        }
     }
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         if (y_is_f32) ((float*)y)[(size_t)t * n + i] = acc[i];
@@ -285,6 +310,9 @@ __global__ void __launch_bounds__(kRvqThreads) rvq_gemm_kernel(const RvqGemmArgs
 
 constexpr int kTcM = 128, kTcN = 32, kTcK = 128;
 constexpr int kTcThreads = 256;
+constexpr int kTcVpt = kTcM * (kTcK / 8) / kTcThreads;   // 8-weight vectors each thread decodes per chunk (8)
+constexpr int kTcBpt = kTcN * kTcK / kTcThreads;         // activations each thread stages per chunk (16)
+static_assert(kTcVpt == 8 && kTcBpt == 16, "thread mapping of rvq_tc_kernel");
 constexpr int kTcLBO = 128;                       // core matrices adjacent along K
 constexpr int kTcSBO = (kTcK / 8) * 128;          // core matrices adjacent along M / N (2048 B)
 constexpr int kTcABytes = kTcM * kTcK * 2;        // 32 KB
@@ -373,8 +401,31 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
             job.n_tok = min(kTcN, a.T_implicit - j * kTcN);
         }
         const int r0 = (tile % a.row_tiles) * kTcM;
+        // per thread: A part (row, half of a chunk's 16 vectors), B part (token, two 8-wide K groups)
+        const int rl = tid >> 1, part = tid & 1;
+        const int arow = r0 + rl;
+        const uint8_t* ip = m.idx + (((size_t)job.matrix * m.rows + (arow < m.rows ? arow : 0)) * nv + part * kTcVpt) * 2;
+        const int bn = tid >> 3, bg = tid & 7;
+        const int bslot = bn < job.n_tok ? (a.slots ? a.slots[job.slot_begin + bn] : job.slot_begin + bn) : -1;
+        const float* bp = a.xr + (size_t)(bslot < 0 ? 0 : bslot) * m.cols + bg * 16;
+        // the global loads of chunk kc + 1 are issued before chunk kc is decoded
+        uint4 pairs_n = arow < m.rows ? __ldg((const uint4*)ip) : make_uint4(0, 0, 0, 0);
+        float4 xv_n[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xv_n[q] = bslot >= 0 ? __ldg((const float4*)bp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int kc = 0; kc < nk; ++kc) {
             const int b = kc & 1;
+            const uint4 pairs = pairs_n;
+            float4 xv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xv[q] = xv_n[q];
+            if (kc + 1 < nk) {
+                if (arow < m.rows) pairs_n = __ldg((const uint4*)(ip + (size_t)(kc + 1) * (kTcK / 8) * 2));
+                if (bslot >= 0) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) xv_n[q] = __ldg((const float4*)(bp + (size_t)(kc + 1) * kTcK) + q);
+                }
+            }
             if (commits[b] > waited[b]) {
                 // the MMAs that last read this buffer must be done before it is rewritten
                 if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
@@ -382,47 +433,29 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
             }
             uint8_t* A = abuf + b * kTcABytes;
             uint8_t* B = bbuf + b * kTcBBytes;
-            // A: thread -> (row, half of the chunk's 16 vectors)
             {
-                const int rl = tid >> 1, half = tid & 1;
-                const int row = r0 + rl;
                 float w[8];
-                uint4 pairs = make_uint4(0, 0, 0, 0);
-                if (row < m.rows) {
-                    const uint8_t* ip = m.idx + (((size_t)job.matrix * m.rows + row) * nv + kc * (kTcK / 8) + half * 8) * 2;
-                    pairs = __ldg((const uint4*)ip);
-                }
                 const uint32_t pw[4] = {pairs.x, pairs.y, pairs.z, pairs.w};
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < kTcVpt; ++q) {
                     const uint32_t pr = (pw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-                    if (row < m.rows) {
+                    if (arow < m.rows) {
                         decode8(scb[pr & 255u], scb[256 + (pr >> 8)], w);
                     } else {
 #pragma unroll
                         for (int z = 0; z < 8; ++z) w[z] = 0.0f;
                     }
-                    const int c8 = half * 8 + q;
+                    const int c8 = part * kTcVpt + q;
                     store_half8(A + (rl >> 3) * kTcSBO + c8 * kTcLBO + (rl & 7) * 16, w);
                 }
             }
-            // B: thread -> (token, two 8-wide K groups)
             {
-                const int n = tid >> 3, g = tid & 7;
-                float v[8];
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c8 = g * 2 + h2;
-                    if (n < job.n_tok) {
-                        const int slot = a.slots ? a.slots[job.slot_begin + n] : job.slot_begin + n;
-                        const float4* src = (const float4*)(a.xr + (size_t)slot * m.cols + kc * kTcK + c8 * 8);
-                        const float4 p0 = src[0], p1 = src[1];
-                        v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
-                        v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
-                    } else {
 #pragma unroll
-                        for (int z = 0; z < 8; ++z) v[z] = 0.0f;
-                    }
-                    store_half8(B + (n >> 3) * kTcSBO + c8 * kTcLBO + (n & 7) * 16, v);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c8 = bg * 2 + h2;
+                    const float v[8] = {xv[2 * h2].x, xv[2 * h2].y, xv[2 * h2].z, xv[2 * h2].w,
+                                        xv[2 * h2 + 1].x, xv[2 * h2 + 1].y, xv[2 * h2 + 1].z, xv[2 * h2 + 1].w};
+                    store_half8(B + (bn >> 3) * kTcSBO + c8 * kTcLBO + (bn & 7) * 16, v);
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -558,6 +591,19 @@ float inv_sqrt(int n) { return (float)(1.0 / std::sqrt((double)n)); }
 
 int fwht_threads(int n) { return std::min(512, std::max(32, n / 2)); }
 
+// Output transform of T tokens with k slots each (slot outputs yp [T*k][n]).
+int launch_out_transform(const float* yp, const int32_t* expert_of, const int8_t* so, const float* gates, int T,
+                         int k, int n, void* y, int y_is_f32, cudaStream_t st) {
+    const int kg = std::max(1, std::min(k, 98304 / (4 * n) - 1));
+    const size_t smem = (size_t)(kg + 1) * n * sizeof(float);
+    int rc = qmoe::cuda_check(cudaFuncSetAttribute(out_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem), "out transform attr");
+    if (rc) return rc;
+    const int threads = std::min(1024, std::max(32, kg * n / 2));
+    out_transform_kernel<<<T, threads, smem, st>>>(yp, expert_of, so, gates, k, kg, n, inv_sqrt(n), y, y_is_f32);
+    return qmoe::launch_check("out_transform_kernel");
+}
+
 }  // namespace
 
 namespace qmoe {
@@ -616,9 +662,7 @@ extern "C" int rvq_expert_matmul(const rvq_matrix_set* mat, const void* x_bf16, 
     if (use_tc(T, cols)) rc = launch_rvq_tc(a, st, (long long)((T + kTcN - 1) / kTcN) * ((rows + kTcM - 1) / kTcM));
     else rc = launch_rvq_gemm(a, st);
     if (rc) return rc;
-    out_transform_kernel<<<T, fwht_threads(rows), 2 * rows * sizeof(float), st>>>(
-        yr, nullptr, mat->sign_out, nullptr, 1, rows, inv_sqrt(rows), y, y_is_f32 ? 1 : 0);
-    return qmoe::launch_check("out_transform_kernel");
+    return launch_out_transform(yr, nullptr, mat->sign_out, nullptr, T, 1, rows, y, y_is_f32 ? 1 : 0, st);
 }
 
 namespace {
@@ -729,9 +773,7 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     a.out = w.dp;
     if ((rc = gemm(a, d_model))) return rc;
     qmoe::phase_event(4, st);
-    out_transform_kernel<<<T, fwht_threads(d_model), 2 * d_model * sizeof(float), st>>>(
-        w.dp, ids, down->sign_out, gates, k, d_model, inv_sqrt(d_model), y, y_is_f32 ? 1 : 0);
-    rc = qmoe::launch_check("out_transform_kernel");
+    rc = launch_out_transform(w.dp, ids, down->sign_out, gates, T, k, d_model, y, y_is_f32 ? 1 : 0, st);
     qmoe::phase_event(5, st);
     return rc;
 }
