@@ -621,6 +621,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling case: keep only this many experts of the c2048-shaped layer")
     ap.add_argument("--tokens", type=int, default=None, help="profiling case: token batch size")
+    ap.add_argument("--rvq-rows", action="store_true",
+                    help="profiling case: only the OLMoE-shaped RVQ layer rows (T=1 and T=32), one JSON line")
     args = ap.parse_args()
     global CFG, T_MAIN, WORKLOAD
     if args.experts or args.tokens:
@@ -652,6 +654,10 @@ def main():
     import torch
     device = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(device)
+    if args.rvq_rows:
+        if rank == 0:
+            print(json.dumps({"workload": "olmoe-rvq rows (profiling case)", "rows": _rvq_rows(device, hbm_peak()[0])}))
+        return 0
     t_setup = time.time()
     layer = build_dict_layer(CFG, device)
     setup_s = time.time() - t_setup
