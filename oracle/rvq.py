@@ -15,7 +15,12 @@ per-row RMS scale and cut into d-dimensional subvectors; each subvector is coded
 by S residual stages, each an 8-bit index into a 256-entry codebook; stage s's
 codebook is k-means-fit on the residual left by earlier stages.  The
 workloads here use d = 8 and S = 2 (2 bits per weight) with fp16 codebooks and
-one codebook pair per layer.
+one codebook set per layer.  [QCA] "Frequency-Conditioned Bit Allocation":
+with an average of S stages, the most-activated third of a layer's experts get
+S + 1 stages and the least-activated third S - 1 (the page's rank-based
+approximation of the reverse-water-filling rates r_e = r + log2(pi_e / pi~) / 2),
+so the mean rate is unchanged; an expert with S_e stages uses the first S_e
+codebooks of the layer's set.
 
 k-means follows the conventions of [M8.5] 0x02B/0x02D: nearest-centroid ties
 go to the lowest index; a cluster that receives no point keeps its previous
@@ -26,7 +31,8 @@ leave them open.
 
 The decoded rotated-basis weight is defined in float32 as
 fp32(s_r) * (fp32(C1[i1]) + fp32(C2[i2])): one add, then one multiply, each
-rounded to nearest even.  The fast Walsh-Hadamard transform is the O(n log n)
+rounded to nearest even; with S stages the adds run left to right,
+((C1 + C2) + C3) ..., and one stage is fp32(s_r) * fp32(C1[i1]).  The fast Walsh-Hadamard transform is the O(n log n)
 butterfly of [M8.5] 0x06C.
 """
 from __future__ import annotations
@@ -143,37 +149,64 @@ def normalised_vectors(wr: np.ndarray, scale_bits: np.ndarray, d: int) -> np.nda
     return (np.asarray(wr, np.float64) / s[:, None]).reshape(rows * (cols // d), d)
 
 
-def fit_codebooks(vectors: np.ndarray, k: int = 256, iters: int = 25, seed: int = 0) -> np.ndarray:
-    """Two residual stages: fp16 codebooks [2, k, d] as float64 values."""
-    c1 = f16_round(kmeans(vectors, k, iters, seed))
-    i1 = nearest(vectors, c1)
-    resid = vectors - c1[i1]
-    c2 = f16_round(kmeans(resid, k, iters, seed + 1))
-    return np.stack([c1, c2])
+def fit_codebooks(vectors: np.ndarray, k: int = 256, iters: int = 25, seed: int = 0, stages: int = 2) -> np.ndarray:
+    """`stages` residual stages: fp16 codebooks [stages, k, d] as float64 values; stage s (seed + s)
+    is fit on what the earlier stages leave, each vector taking its nearest rounded codeword."""
+    cbs = []
+    resid = np.asarray(vectors, np.float64)
+    for st in range(stages):
+        c = f16_round(kmeans(resid, k, iters, seed + st))
+        resid = resid - c[nearest(resid, c)]
+        cbs.append(c)
+    return np.stack(cbs)
 
 
-def encode(wr: np.ndarray, codebooks: np.ndarray, d: int = 8):
-    """Indices uint8 [rows, cols/d, 2] and fp16 scale bits [rows] of a rotated weight."""
+def encode(wr: np.ndarray, codebooks: np.ndarray, d: int = 8, stages: int | None = None):
+    """Indices uint8 [rows, cols/d, S] and fp16 scale bits [rows] of a rotated weight, S = stages
+    (default: every codebook of the set): stage s takes the codeword nearest to what stages
+    0 .. s-1 leave of u."""
     rows, cols = wr.shape
-    scale = row_scale_f16(wr)
-    u = normalised_vectors(wr, scale, d)
     cb = np.asarray(codebooks, np.float64)
-    i1 = nearest(u, cb[0])
-    i2 = nearest(u - cb[0][i1], cb[1])
-    idx = np.stack([i1, i2], axis=1).astype(np.uint8).reshape(rows, cols // d, 2)
-    return idx, scale
+    n_st = cb.shape[0] if stages is None else stages
+    if not 1 <= n_st <= cb.shape[0]:
+        raise ValueError("stage count outside 1 .. number of codebooks")
+    scale = row_scale_f16(wr)
+    resid = normalised_vectors(wr, scale, d)
+    idx = []
+    for st in range(n_st):
+        i = nearest(resid, cb[st])
+        idx.append(i)
+        resid = resid - cb[st][i]
+    return np.stack(idx, axis=1).astype(np.uint8).reshape(rows, cols // d, n_st), scale
 
 
 def decode(idx: np.ndarray, codebooks_f16_bits: np.ndarray, scale_bits: np.ndarray) -> np.ndarray:
-    """Decoded rotated-basis weight, float32 [rows, cols]: fp32(s) * (fp32(C1[i1]) + fp32(C2[i2]))."""
+    """Decoded rotated-basis weight, float32 [rows, cols]:
+    fp32(s) * (((fp32(C1[i1]) + fp32(C2[i2])) + fp32(C3[i3])) ...), as many stages as idx holds."""
     idx = np.asarray(idx)
-    rows, nv, _ = idx.shape
+    rows, nv, n_st = idx.shape
     cb = np.asarray(codebooks_f16_bits, np.uint16).view(np.float16).astype(np.float32)
     d = cb.shape[2]
     s = np.asarray(scale_bits, np.uint16).view(np.float16).astype(np.float32)
-    summed = cb[0][idx[:, :, 0]] + cb[1][idx[:, :, 1]]            # float32 add
+    summed = cb[0][idx[:, :, 0]]
+    for st in range(1, n_st):
+        summed = summed + cb[st][idx[:, :, st]]                      # float32 adds, left to right
     w = s[:, None, None] * summed                                    # float32 multiply
     return w.reshape(rows, nv * d).astype(np.float32)
+
+
+def stage_allocation(popularity: np.ndarray, s_bar: int) -> np.ndarray:
+    """Stages per expert ([QCA] "Frequency-Conditioned Bit Allocation", rank-based form):
+    the floor(E/3) most popular experts get s_bar + 1, the floor(E/3) least popular s_bar - 1, the
+    rest s_bar.  Equal popularity ranks the lower expert id as more popular."""
+    pop = np.asarray(popularity, np.float64)
+    E = pop.shape[0]
+    third = E // 3
+    order = sorted(range(E), key=lambda e: (-pop[e], e))
+    st = np.full(E, s_bar, dtype=np.int64)
+    st[order[:third]] = s_bar + 1
+    st[order[E - third:]] = s_bar - 1
+    return st
 
 
 def linear(x: np.ndarray, w_dec: np.ndarray, sign_out: np.ndarray, sign_in: np.ndarray) -> np.ndarray:

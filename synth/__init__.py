@@ -39,6 +39,7 @@ TAG_ZIPF = 5
 TAG_RVQ_W = 6
 TAG_RVQ_SIGN = 7
 TAG_KMEANS = 8
+TAG_ZIPF_RANK = 9
 
 
 def splitmix64_scalar(key: int, idx: int) -> int:
@@ -150,6 +151,27 @@ def zipf_logits(seed: int, T: int, E: int, s: float) -> np.ndarray:
     return (base[None, :] + gumbel).astype(np.float32)
 
 
+def zipf_popularity(seed: int, E: int, s: float) -> np.ndarray:
+    """Selection weights pi_e ~ rank**-s of a layer's experts, summing to 1; ranks map to
+    expert ids through a seeded permutation that belongs to the layer (not to a batch)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, TAG_ZIPF_RANK, E]))
+    perm = rng.permutation(E)             # perm[rank-1] = expert id
+    pi = np.arange(1, E + 1, dtype=np.float64) ** -s
+    pi /= pi.sum()
+    out = np.empty(E, dtype=np.float64)
+    out[perm] = pi
+    return out
+
+
+def zipf_layer_logits(seed: int, T: int, E: int, s: float) -> np.ndarray:
+    """Router logits log pi_e + Gumbel(0,1) noise with the layer's fixed popularity
+    (zipf_popularity): top-k picks experts without replacement with P ~ pi.  float32 [T, E]."""
+    logpi = np.log(zipf_popularity(seed, E, s))
+    rng = np.random.default_rng(np.random.SeedSequence([seed, TAG_ZIPF_RANK, T, E]))
+    u = np.clip(rng.random((T, E)), 1e-300, None)
+    return (logpi[None, :] - np.log(-np.log(u))).astype(np.float32)
+
+
 def normal_logits(seed: int, T: int, E: int) -> np.ndarray:
     rng = np.random.default_rng(np.random.SeedSequence([seed, TAG_LOGITS, T, E]))
     return rng.standard_normal((T, E)).astype(np.float32)
@@ -210,6 +232,9 @@ class RvqLayer:
     vec_dim: int = 8
     stages: int = 2
     codebook_size: int = 256
+    # frequency-conditioned stages: router with the layer's fixed Zipf popularity, and per-expert
+    # stage counts stages-1 / stages / stages+1 for the least / middle / most popular thirds
+    freq_stages: bool = False
 
 
 LINEAR_1024x4096 = LinearCfg("linear-1024x4096-p0.89", 1024, 4096, 0.89, 0, (1, 8, 32))
@@ -217,6 +242,7 @@ SWITCH_BASE_128 = DictLayer("switch-base-128", 128, 768, 3072, 0.857, 1, 1, "nor
 SWITCH_LARGE_128 = DictLayer("switch-large-128", 128, 1024, 4096, 0.87, 2, 1, "zipf", 1.1, (2048,))
 SWITCH_C2048 = DictLayer("switch-c2048", 2048, 2080, 6144, 0.886, 3, 1, "zipf", 1.0, (1, 64, 4096))
 OLMOE_RVQ = RvqLayer("olmoe-rvq-2bit", 64, 2048, 1024, 4, 8, 0.9, (1, 32))
+OLMOE_RVQ_FREQ = RvqLayer("olmoe-rvq-freq-2bit", 64, 2048, 1024, 4, 8, 0.9, (1, 32), freq_stages=True)
 
 # matrix ids inside a dictionary-coded expert
 WI, WO = 0, 1
@@ -236,6 +262,8 @@ def rvq_matrix_shape(cfg: RvqLayer, matrix: int) -> tuple[int, int]:
 def layer_logits(cfg, T: int) -> np.ndarray:
     if getattr(cfg, "routing", "zipf") == "normal":
         return normal_logits(cfg.seed, T, cfg.E)
+    if getattr(cfg, "freq_stages", False):
+        return zipf_layer_logits(cfg.seed, T, cfg.E, cfg.zipf_s)
     return zipf_logits(cfg.seed, T, cfg.E, cfg.zipf_s)
 
 

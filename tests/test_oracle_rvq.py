@@ -114,3 +114,85 @@ def test_silu_closed_form():
     assert R.silu(np.array([0.0]))[0] == 0.0
     assert np.isclose(R.silu(np.array([1.0]))[0], 1.0 / (1.0 + np.exp(-1.0)))
     assert np.isclose(R.silu(np.array([-20.0]))[0], -20.0 * np.exp(-20.0) / (1 + np.exp(-20.0)))
+
+
+# ------------------------------------------------------ frequency-conditioned stages
+def test_stage_allocation_thirds_by_rank():
+    """E = 64, s = 2: the 21 most popular experts (ranks 1..21 of the layer's Zipf order) get 3
+    stages, the 21 least popular 1, the 22 others 2; the mean is exactly 2 (rate-matched)."""
+    cfg = synth.OLMOE_RVQ_FREQ
+    pop = synth.zipf_popularity(cfg.seed, cfg.E, cfg.zipf_s)
+    st = R.stage_allocation(pop, cfg.stages)
+    # the layer's rank -> expert order, rebuilt from the generator's permutation
+    rng = np.random.default_rng(np.random.SeedSequence([cfg.seed, synth.TAG_ZIPF_RANK, cfg.E]))
+    perm = rng.permutation(cfg.E)
+    assert sorted(np.nonzero(st == 3)[0].tolist()) == sorted(perm[:21].tolist())
+    assert sorted(np.nonzero(st == 1)[0].tolist()) == sorted(perm[-21:].tolist())
+    assert (st == 2).sum() == 22
+    assert st.sum() == 2 * cfg.E
+
+
+def test_stage_allocation_follows_water_filling_order():
+    """The reverse-water-filling rates r_e = r + log2(pi_e / geomean(pi)) / 2 order experts the same
+    way: every 3-stage expert has a higher rate than every 2-stage one, and so on."""
+    pop = np.random.default_rng(3).dirichlet(np.ones(30))
+    st = R.stage_allocation(pop, 2)
+    r = 2 + 0.5 * np.log2(pop / np.exp(np.mean(np.log(pop))))
+    for hi, lo in ((3, 2), (2, 1)):
+        assert r[st == hi].min() > r[st == lo].max()
+    assert st.sum() == 60
+
+
+def test_stage_allocation_ties_and_small_layers():
+    assert R.stage_allocation(np.ones(6), 2).tolist() == [3, 3, 2, 2, 1, 1]
+    assert R.stage_allocation(np.ones(2), 2).tolist() == [2, 2]      # floor(2/3) = 0 per third
+
+
+def test_one_stage_decode_is_scale_times_first_codeword():
+    rng = np.random.default_rng(5)
+    cb = (rng.standard_normal((3, 256, 8)) * 0.3).astype(np.float16)
+    idx = rng.integers(0, 256, size=(4, 3, 1)).astype(np.uint8)
+    sc = np.array([0.5, 1.25, 0.01, 3.0], np.float16)
+    w = R.decode(idx, cb.view(np.uint16), sc.view(np.uint16))
+    for r in range(4):
+        for v in range(3):
+            exp = np.float32(sc[r]) * cb[0][idx[r, v, 0]].astype(np.float32)
+            assert np.array_equal(w[r, 8 * v:8 * v + 8], exp)
+
+
+def test_three_stage_decode_with_zero_third_codebook_equals_two_stage():
+    rng = np.random.default_rng(6)
+    cb = (rng.standard_normal((3, 256, 8)) * 0.3).astype(np.float16)
+    cb[2] = 0
+    idx3 = rng.integers(0, 256, size=(5, 4, 3)).astype(np.uint8)
+    sc = (rng.random(5) + 0.1).astype(np.float16)
+    w3 = R.decode(idx3, cb.view(np.uint16), sc.view(np.uint16))
+    w2 = R.decode(idx3[:, :, :2], cb[:2].view(np.uint16), sc.view(np.uint16))
+    assert np.array_equal(w3, w2)
+    # explicit float32 sums, left to right
+    c = cb.astype(np.float32)
+    exp = np.float32(sc[1]) * ((c[0][idx3[1, 2, 0]] + c[1][idx3[1, 2, 1]]) + c[2][idx3[1, 2, 2]])
+    assert np.array_equal(w3[1, 16:24], exp)
+
+
+def test_encode_prefix_consistency_across_stage_counts():
+    """Stage s's index depends only on stages before it: the S-stage code is a prefix of the
+    (S+1)-stage code, and a 2-codebook set gives the same first two stages as a 3-codebook set."""
+    cfg = synth.OLMOE_RVQ
+    w = synth.rvq_weight(cfg.seed, 0, synth.GATE, 16, 64)
+    so, si = synth.rvq_signs(cfg.seed, 0, synth.GATE, 16, 64)
+    wr = R.rotate_weight(w, so, si)
+    u = R.normalised_vectors(wr, R.row_scale_f16(wr), 8)
+    cb3 = R.fit_codebooks(u, k=16, iters=5, seed=1, stages=3)
+    cb2 = R.fit_codebooks(u, k=16, iters=5, seed=1, stages=2)
+    assert np.array_equal(cb3[:2], cb2)
+    i1, _ = R.encode(wr, cb3, stages=1)
+    i2, _ = R.encode(wr, cb2)
+    i3, _ = R.encode(wr, cb3)
+    assert np.array_equal(i3[:, :, :2], i2) and np.array_equal(i2[:, :, :1], i1)
+    # more stages never leave a larger total squared error on the fitted data
+    errs = []
+    for idx in (i1, i2, i3):
+        d = R.decode(idx, R.f16_round(cb3).astype(np.float16).view(np.uint16), R.row_scale_f16(wr))
+        errs.append(float(np.sum((d - wr) ** 2)))
+    assert errs[0] > errs[1] > errs[2]
