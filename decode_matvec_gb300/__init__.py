@@ -32,7 +32,8 @@ EXPORTED = [
     "qmoe_bucketise", "qmoe_moe_layer_ws_size", "qmoe_moe_layer", "rvq_expert_matmul_ws_size",
     "rvq_expert_matmul", "rvq_moe_layer_ws_size", "rvq_moe_layer", "rvq_pack", "qmoe_check_status",
     "qmoe_last_error", "qmoe_decode_dense", "rvq_decode_dense", "qmoe_set_phase_events",
-    "qmoe_moe_layer_noalloc", "qmoe_pack_device_ws_size", "qmoe_pack_device",
+    "qmoe_moe_layer_noalloc", "qmoe_pack_device_ws_size", "qmoe_pack_device", "rvq_pack_stages",
+    "rvq_stage_allocation",
 ]
 
 
@@ -62,7 +63,8 @@ class CMatrixSet(ctypes.Structure):
 class CRvqSet(ctypes.Structure):
     _fields_ = [("idx", ctypes.c_void_p), ("codebooks", ctypes.c_void_p), ("scale_f16", ctypes.c_void_p),
                 ("sign_out", ctypes.c_void_p), ("sign_in", ctypes.c_void_p), ("count", ctypes.c_int),
-                ("rows", ctypes.c_int), ("cols", ctypes.c_int)]
+                ("rows", ctypes.c_int), ("cols", ctypes.c_int), ("stages", ctypes.c_void_p),
+                ("idx_base", ctypes.c_void_p), ("n_stages", ctypes.c_int)]
 
 
 _vp, _i, _sz, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
@@ -87,6 +89,8 @@ _sig = {
     "qmoe_moe_layer_noalloc": [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _vp],
     "qmoe_pack_device_ws_size": [_i, _i, _i, _vp],
     "qmoe_pack_device": [_vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp, _sz, _vp],
+    "rvq_pack_stages": [_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _vp],
+    "rvq_stage_allocation": [_vp, _i, _i, _vp],
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -161,18 +165,31 @@ def qmoe_dict_compact(dict_words: np.ndarray) -> np.ndarray:
     return out
 
 
-def rvq_pack(w: np.ndarray, sign_out: np.ndarray, sign_in: np.ndarray, codebooks_f16: np.ndarray):
-    """Host RVQ encoder: (idx uint8 [rows, cols/8, 2], scale fp16 bits [rows])."""
+def rvq_pack(w: np.ndarray, sign_out: np.ndarray, sign_in: np.ndarray, codebooks_f16: np.ndarray,
+             stages: int | None = None):
+    """Host RVQ encoder: (idx uint8 [rows, cols/8, S], scale fp16 bits [rows]); S = stages, by default
+    the number of codebooks given ([S_max, 256, 8] fp16 bits; the first S are used)."""
     w = np.ascontiguousarray(w, dtype=np.float64)
     rows, cols = w.shape
     so = np.ascontiguousarray(sign_out, dtype=np.int8)
     si = np.ascontiguousarray(sign_in, dtype=np.int8)
     cb = np.ascontiguousarray(codebooks_f16, dtype=np.uint16)
-    idx = np.zeros((rows, cols // 8, 2), dtype=np.uint8)
+    n_st = cb.shape[0] if stages is None else int(stages)
+    if not 1 <= n_st <= cb.shape[0]:
+        raise ValueError("stage count outside 1 .. number of codebooks")
+    idx = np.zeros((rows, cols // 8, n_st), dtype=np.uint8)
     sc = np.zeros(rows, dtype=np.uint16)
-    _check(_lib.rvq_pack(_np_ptr(w), rows, cols, _np_ptr(so), _np_ptr(si), _np_ptr(cb), _np_ptr(idx), _np_ptr(sc)),
-           "rvq_pack")
+    _check(_lib.rvq_pack_stages(_np_ptr(w), rows, cols, _np_ptr(so), _np_ptr(si), _np_ptr(cb), n_st, _np_ptr(idx),
+                                _np_ptr(sc)), "rvq_pack_stages")
     return idx, sc
+
+
+def rvq_stage_allocation(popularity: np.ndarray, s_bar: int = 2) -> np.ndarray:
+    """Stages per expert by popularity thirds (s_bar + 1 / s_bar / s_bar - 1), uint8 [E]."""
+    pop = np.ascontiguousarray(popularity, dtype=np.float64)
+    out = np.zeros(pop.shape[0], dtype=np.uint8)
+    _check(_lib.rvq_stage_allocation(_np_ptr(pop), pop.shape[0], int(s_bar), _np_ptr(out)), "rvq_stage_allocation")
+    return out
 
 
 def qmoe_last_error() -> str:
@@ -223,21 +240,43 @@ class MatrixSet:
 
 
 class RvqMatrixSet:
-    def __init__(self, idx, codebooks, scale_f16, sign_out, sign_in, count, rows, cols):
+    """`count` RVQ-coded matrices of one shape, resident on the device.  With `stages` (device uint8 per
+    matrix) and `idx_base` (device int64 byte offsets), matrices may have 1 .. n_stages stages each."""
+
+    def __init__(self, idx, codebooks, scale_f16, sign_out, sign_in, count, rows, cols, stages=None, idx_base=None,
+                 n_stages=0):
         self.idx, self.codebooks, self.scale, self.sign_out, self.sign_in = idx, codebooks, scale_f16, sign_out, sign_in
         self.count, self.rows, self.cols = count, rows, cols
+        self.stages, self.idx_base, self.n_stages = stages, idx_base, n_stages
         self.c = CRvqSet(_dptr(idx), _dptr(codebooks), _dptr(scale_f16), _dptr(sign_out), _dptr(sign_in), count,
-                         rows, cols)
+                         rows, cols, _dptr(stages), _dptr(idx_base), n_stages)
 
     @classmethod
     def from_host(cls, idx, codebooks_f16, scale_f16, sign_out, sign_in, count, rows, cols, device="cuda"):
+        """idx: uint8 [count, rows, cols/8, 2] (two stages each), or a list of count arrays
+        [rows, cols/8, S_e] with per-matrix stage counts (each matrix's codes start 16-byte aligned)."""
         import torch
 
         def up(a, dt, view):
             return torch.from_numpy(np.ascontiguousarray(a, dtype=dt).view(view).copy()).to(device)
-        return cls(up(idx, np.uint8, np.uint8), up(codebooks_f16, np.uint16, np.int16),
+        cb = np.ascontiguousarray(codebooks_f16, dtype=np.uint16)
+        if isinstance(idx, (list, tuple)):
+            st = np.array([a.shape[2] for a in idx], dtype=np.uint8)
+            sizes = [a.size for a in idx]
+            base = np.zeros(count, dtype=np.int64)
+            off = 0
+            for e, n in enumerate(sizes):
+                base[e] = off
+                off += (n + 15) // 16 * 16
+            flat = np.zeros(max(off, 16), dtype=np.uint8)
+            for e, a in enumerate(idx):
+                flat[base[e]:base[e] + sizes[e]] = np.ascontiguousarray(a, dtype=np.uint8).reshape(-1)
+            return cls(up(flat, np.uint8, np.uint8), up(cb, np.uint16, np.int16), up(scale_f16, np.uint16, np.int16),
+                       up(sign_out, np.int8, np.int8), up(sign_in, np.int8, np.int8), count, rows, cols,
+                       stages=up(st, np.uint8, np.uint8), idx_base=up(base, np.int64, np.int64), n_stages=cb.shape[0])
+        return cls(up(idx, np.uint8, np.uint8), up(cb, np.uint16, np.int16),
                    up(scale_f16, np.uint16, np.int16), up(sign_out, np.int8, np.int8), up(sign_in, np.int8, np.int8),
-                   count, rows, cols)
+                   count, rows, cols, n_stages=cb.shape[0])
 
 
 # ================================================================ device calls

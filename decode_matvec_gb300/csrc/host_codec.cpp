@@ -351,14 +351,16 @@ bool pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
 }  // namespace
 
-extern "C" int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_out,
-                        const int8_t* sign_in, const uint16_t* codebooks, uint8_t* idx,
-                        uint16_t* scale_f16) {
+extern "C" int rvq_pack_stages(const double* w, int rows, int cols, const int8_t* sign_out,
+                               const int8_t* sign_in, const uint16_t* codebooks, int n_stages, uint8_t* idx,
+                               uint16_t* scale_f16) {
     qmoe::clear_error();
     if (!w || !sign_out || !sign_in || !codebooks || !idx || !scale_f16)
         return fail(QMOE_EINVAL, "rvq_pack: NULL argument");
     if (!pow2(rows) || !pow2(cols) || cols % 8 || rows > 8192 || cols > 8192)
         return fail(QMOE_EINVAL, "rvq_pack: rows and cols must be powers of two in [8, 8192]");
+    if (n_stages < 1 || n_stages > QMOE_RVQ_MAX_STAGES)
+        return fail(QMOE_EINVAL, "rvq_pack: stage count outside 1 .. QMOE_RVQ_MAX_STAGES");
     std::vector<double> a((size_t)rows * cols);
     for (int r = 0; r < rows; ++r)
         for (int c = 0; c < cols; ++c) {
@@ -368,9 +370,8 @@ extern "C" int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_
         }
     for (int c = 0; c < cols; ++c) fwht_strided(a.data() + c, rows, (size_t)cols);
     for (int r = 0; r < rows; ++r) fwht_strided(a.data() + (size_t)r * cols, cols, 1);
-    double cb[2][QMOE_RVQ_CODES * 8];
-    for (int s = 0; s < 2; ++s)
-        for (int i = 0; i < QMOE_RVQ_CODES * 8; ++i) cb[s][i] = half_to_double(codebooks[s * QMOE_RVQ_CODES * 8 + i]);
+    std::vector<double> cb((size_t)n_stages * QMOE_RVQ_CODES * 8);
+    for (size_t i = 0; i < cb.size(); ++i) cb[i] = half_to_double(codebooks[i]);
     for (int r = 0; r < rows; ++r) {
         const double* row = a.data() + (size_t)r * cols;
         double sum = 0.0;
@@ -380,14 +381,38 @@ extern "C" int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_
         if (s == 0.0) return fail(QMOE_EINVAL, "rvq_pack: a row's scale rounds to zero");
         scale_f16[r] = sh;
         for (int v = 0; v < cols / 8; ++v) {
-            double u[8], res[8];
-            for (int k = 0; k < 8; ++k) u[k] = row[v * 8 + k] / s;
-            int i1 = nearest8(u, cb[0]);
-            for (int k = 0; k < 8; ++k) res[k] = u[k] - cb[0][i1 * 8 + k];
-            int i2 = nearest8(res, cb[1]);
-            idx[((size_t)r * (cols / 8) + v) * 2] = (uint8_t)i1;
-            idx[((size_t)r * (cols / 8) + v) * 2 + 1] = (uint8_t)i2;
+            double res[8];
+            for (int k = 0; k < 8; ++k) res[k] = row[v * 8 + k] / s;
+            for (int st = 0; st < n_stages; ++st) {
+                const double* c = cb.data() + (size_t)st * QMOE_RVQ_CODES * 8;
+                const int i = nearest8(res, c);
+                for (int k = 0; k < 8; ++k) res[k] = res[k] - c[i * 8 + k];
+                idx[((size_t)r * (cols / 8) + v) * n_stages + st] = (uint8_t)i;
+            }
         }
+    }
+    return QMOE_OK;
+}
+
+extern "C" int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_out,
+                        const int8_t* sign_in, const uint16_t* codebooks, uint8_t* idx,
+                        uint16_t* scale_f16) {
+    return rvq_pack_stages(w, rows, cols, sign_out, sign_in, codebooks, 2, idx, scale_f16);
+}
+
+extern "C" int rvq_stage_allocation(const double* popularity, int E, int s_bar, uint8_t* stages) {
+    qmoe::clear_error();
+    if (!popularity || !stages || E < 1) return fail(QMOE_EINVAL, "rvq_stage_allocation: NULL argument or E < 1");
+    const int third = E / 3;
+    if (s_bar < 1 || s_bar > QMOE_RVQ_MAX_STAGES || (third > 0 && (s_bar < 2 || s_bar + 1 > QMOE_RVQ_MAX_STAGES)))
+        return fail(QMOE_EINVAL, "rvq_stage_allocation: s_bar - 1 and s_bar + 1 must be valid stage counts");
+    std::vector<int> order(E);
+    for (int e = 0; e < E; ++e) order[e] = e;
+    // most popular first; equal popularity: lower expert id first
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return popularity[x] > popularity[y]; });
+    for (int q = 0; q < E; ++q) {
+        const int e = order[q];
+        stages[e] = (uint8_t)(q < third ? s_bar + 1 : q >= E - third ? s_bar - 1 : s_bar);
     }
     return QMOE_OK;
 }

@@ -34,17 +34,40 @@ struct RvqDev {
     const int8_t* so;
     const int8_t* si;
     int count, rows, cols;
+    const uint8_t* stages;     // per matrix stage count, or NULL (2)
+    const uint64_t* idx_base;  // per matrix byte offset of its codes, or NULL
+    int n_st;                  // codebooks in the set
 };
 
 RvqDev to_dev(const rvq_matrix_set* s) {
-    return RvqDev{s->idx, s->codebooks, s->scale_f16, s->sign_out, s->sign_in, s->count, s->rows, s->cols};
+    return RvqDev{s->idx, s->codebooks, s->scale_f16, s->sign_out, s->sign_in, s->count, s->rows, s->cols,
+                  s->stages, s->idx_base, s->n_stages ? s->n_stages : 2};
+}
+
+// Stage count of matrix e, or 0 for a count outside 1 .. n_st: that records
+// QMOE_EFORMAT, and the kernels then read none of the matrix's codes (its
+// layout is unknown) and leave its outputs unwritten (decode: zeros).
+__device__ __forceinline__ int stages_of(const RvqDev& m, int e) {
+    if (!m.stages) return 2;
+    const int st = m.stages[e];
+    if (st < 1 || st > m.n_st) {
+        atomicCAS(&g_rvq_error, 0, QMOE_EFORMAT);
+        return 0;
+    }
+    return st;
+}
+
+// First code byte of matrix e: [rows][cols/8][stages] bytes from here.
+__device__ __forceinline__ const uint8_t* codes_of(const RvqDev& m, int e) {
+    return m.idx + (m.idx_base ? m.idx_base[e] : (uint64_t)e * m.rows * (m.cols / 8) * 2);
 }
 
 bool pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
 bool valid_set(const rvq_matrix_set* s) {
     return s && s->idx && s->codebooks && s->scale_f16 && s->sign_out && s->sign_in && s->count >= 1 &&
-           pow2(s->rows) && pow2(s->cols) && s->cols >= 8 && s->rows <= 8192 && s->cols <= 8192;
+           pow2(s->rows) && pow2(s->cols) && s->cols >= 8 && s->rows <= 8192 && s->cols <= 8192 &&
+           s->n_stages >= 0 && s->n_stages <= QMOE_RVQ_MAX_STAGES && (s->stages || s->n_stages != 1);
 }
 
 // Normalised Walsh-Hadamard transform of n floats in shared memory, in place.
@@ -182,33 +205,54 @@ struct RvqGemmArgs {
     float* out;           // rotated outputs, fp32 [slot][rows]
 };
 
-__device__ __forceinline__ void decode8(uint4 c1, uint4 c2, float (&w)[8]) {
+// w = C1 (+ C2 (+ C3)) of one 8-weight vector, fp32 adds left to right.
+template <int S>
+__device__ __forceinline__ void decode_vec(const uint4* cb, const uint32_t (&code)[S], float (&w)[8]) {
+    const uint4 c1 = cb[code[0]];
     const uint32_t a[4] = {c1.x, c1.y, c1.z, c1.w};
-    const uint32_t b[4] = {c2.x, c2.y, c2.z, c2.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&a[q]));
-        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&b[q]));
-        w[2 * q] = fa.x + fb.x;
-        w[2 * q + 1] = fa.y + fb.y;
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&a[q]));
+        w[2 * q] = f.x;
+        w[2 * q + 1] = f.y;
+    }
+#pragma unroll
+    for (int st = 1; st < S; ++st) {
+        const uint4 c = cb[256 * st + code[st]];
+        const uint32_t b[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&b[q]));
+            w[2 * q] = w[2 * q] + f.x;
+            w[2 * q + 1] = w[2 * q + 1] + f.y;
+        }
     }
 }
 
-template <int NT>
+template <int NT, int S>
 __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const float* xs, const Job& job, int r0,
                               int warp, int nwarps, int lane) {
     const RvqDev& m = a.m;
     const int nv = m.cols / 8;
     const int r1 = min(m.rows, r0 + a.rows_per_tile);
+    const uint8_t* codes = codes_of(m, job.matrix);
     for (int r = r0 + warp; r < r1; r += nwarps) {
-        const uint16_t* ip = (const uint16_t*)(m.idx + ((size_t)job.matrix * m.rows + r) * nv * 2);
+        const uint8_t* ip = codes + (size_t)r * nv * S;
         float acc[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
         for (int v = lane; v < nv; v += 32) {
-            const uint32_t pr = __ldg(ip + v);
+            uint32_t code[S];
+            if constexpr (S == 2) {
+                const uint32_t pr = __ldg((const uint16_t*)ip + v);
+                code[0] = pr & 255u;
+                code[1] = pr >> 8;
+            } else {
+#pragma unroll
+                for (int st = 0; st < S; ++st) code[st] = __ldg(ip + (size_t)v * S + st);
+            }
             float w[8];
-            decode8(scb[pr & 255u], scb[256 + (pr >> 8)], w);
+            decode_vec<S>(scb, code, w);
             if constexpr (NT == 1) {
                 const float4 x0 = ((const float4*)xs)[2 * v], x1 = ((const float4*)xs)[2 * v + 1];
                 acc[0] = fmaf(w[0], x0.x, acc[0]);
@@ -220,17 +264,19 @@ __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const floa
                 acc[0] = fmaf(w[6], x1.z, acc[0]);
                 acc[0] = fmaf(w[7], x1.w, acc[0]);
             } else {
+                // activations staged [token][column]: a lane's 8 columns are 32 contiguous bytes
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float* xc = xs + (size_t)(8 * v + j) * NT;
-#pragma unroll
-                    for (int t = 0; t < NT; t += 4) {
-                        const float4 xv = *(const float4*)(xc + t);
-                        acc[t] = fmaf(w[j], xv.x, acc[t]);
-                        if (t + 1 < NT) acc[t + 1] = fmaf(w[j], xv.y, acc[t + 1]);
-                        if (t + 2 < NT) acc[t + 2] = fmaf(w[j], xv.z, acc[t + 2]);
-                        if (t + 3 < NT) acc[t + 3] = fmaf(w[j], xv.w, acc[t + 3]);
-                    }
+                for (int t = 0; t < NT; ++t) {
+                    const float4* xt = (const float4*)(xs + (size_t)t * m.cols) + 2 * v;
+                    const float4 x0 = xt[0], x1 = xt[1];
+                    acc[t] = fmaf(w[0], x0.x, acc[t]);
+                    acc[t] = fmaf(w[1], x0.y, acc[t]);
+                    acc[t] = fmaf(w[2], x0.z, acc[t]);
+                    acc[t] = fmaf(w[3], x0.w, acc[t]);
+                    acc[t] = fmaf(w[4], x1.x, acc[t]);
+                    acc[t] = fmaf(w[5], x1.y, acc[t]);
+                    acc[t] = fmaf(w[6], x1.z, acc[t]);
+                    acc[t] = fmaf(w[7], x1.w, acc[t]);
                 }
             }
         }
@@ -255,23 +301,28 @@ __device__ void rvq_stage(const RvqGemmArgs& a, const Job& job, float* xs) {
         if (t < job.n_tok) {
             const int slot = a.slots ? a.slots[job.slot_begin + t] : job.slot_begin + t;
             const float* src = a.xr + (size_t)slot * cols;
-            for (int c = threadIdx.x; c < cols; c += blockDim.x) xs[(size_t)c * NT + t] = src[c];
+            for (int c = threadIdx.x; c < cols; c += blockDim.x) xs[(size_t)t * cols + c] = src[c];
         } else {
-            for (int c = threadIdx.x; c < cols; c += blockDim.x) xs[(size_t)c * NT + t] = 0.0f;
+            for (int c = threadIdx.x; c < cols; c += blockDim.x) xs[(size_t)t * cols + c] = 0.0f;
         }
     }
 }
 
 __global__ void __launch_bounds__(kRvqThreads) rvq_gemm_kernel(const RvqGemmArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    uint4* scb = (uint4*)smem;                  // [2][256] x 8 fp16
-    float* xs = (float*)(smem + 2 * 256 * 16);
+    uint4* scb = (uint4*)smem;                  // [n_st][256] x 8 fp16
+    float* xs = (float*)(smem + (size_t)a.m.n_st * 256 * 16);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int i = tid; i < 2 * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)a.m.cb + i);
+    for (int i = tid; i < a.m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)a.m.cb + i);
     __syncthreads();
     const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
     const int n_tiles = n_jobs * a.row_tiles;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    // each block takes a contiguous range of tiles: consecutive row ranges of one job reuse the
+    // staged activations
+    const int per_block = (n_tiles + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per_block, t_end = min(n_tiles, t_begin + per_block);
+    int staged = -1;
+    for (int tile = t_begin; tile < t_end; ++tile) {
         Job job;
         const int j = tile / a.row_tiles;
         if (a.jobs) {
@@ -283,13 +334,29 @@ __global__ void __launch_bounds__(kRvqThreads) rvq_gemm_kernel(const RvqGemmArgs
         }
         const int r0 = (tile % a.row_tiles) * a.rows_per_tile;
         const int nt = job.n_tok <= 1 ? 1 : job.n_tok <= 4 ? 4 : 8;
-        if (nt == 1) rvq_stage<1>(a, job, xs);
-        else if (nt == 4) rvq_stage<4>(a, job, xs);
-        else rvq_stage<8>(a, job, xs);
+        if (j != staged) {
+            if (nt == 1) rvq_stage<1>(a, job, xs);
+            else if (nt == 4) rvq_stage<4>(a, job, xs);
+            else rvq_stage<8>(a, job, xs);
+            staged = j;
+        }
         __syncthreads();
-        if (nt == 1) rvq_tile_rows<1>(a, scb, xs, job, r0, warp, nwarps, lane);
-        else if (nt == 4) rvq_tile_rows<4>(a, scb, xs, job, r0, warp, nwarps, lane);
-        else rvq_tile_rows<8>(a, scb, xs, job, r0, warp, nwarps, lane);
+        const int S = stages_of(a.m, job.matrix);
+        if (S == 0) {
+            // nothing
+        } else if (S == 2) {
+            if (nt == 1) rvq_tile_rows<1, 2>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else if (nt == 4) rvq_tile_rows<4, 2>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else rvq_tile_rows<8, 2>(a, scb, xs, job, r0, warp, nwarps, lane);
+        } else if (S == 1) {
+            if (nt == 1) rvq_tile_rows<1, 1>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else if (nt == 4) rvq_tile_rows<4, 1>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else rvq_tile_rows<8, 1>(a, scb, xs, job, r0, warp, nwarps, lane);
+        } else {
+            if (nt == 1) rvq_tile_rows<1, 3>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else if (nt == 4) rvq_tile_rows<4, 3>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else rvq_tile_rows<8, 3>(a, scb, xs, job, r0, warp, nwarps, lane);
+        }
         __syncthreads();
     }
 }
@@ -317,7 +384,9 @@ constexpr int kTcLBO = 128;                       // core matrices adjacent alon
 constexpr int kTcSBO = (kTcK / 8) * 128;          // core matrices adjacent along M / N (2048 B)
 constexpr int kTcABytes = kTcM * kTcK * 2;        // 32 KB
 constexpr int kTcBBytes = kTcN * kTcK * 2;        // 8 KB
-constexpr int kTcSmem = 1024 /*align*/ + 2 * 256 * 16 /*codebooks*/ + 2 * (kTcABytes + kTcBBytes) + 64;
+constexpr int kTcCbBytes = QMOE_RVQ_MAX_STAGES * 256 * 16;
+// two weight tiles (steps alternate), and per chunk parity the activations' fp16 high and low parts
+constexpr int kTcSmem = 1024 /*align*/ + kTcCbBytes + 2 * kTcABytes + 4 * kTcBBytes + 64;
 constexpr uint32_t kTcSpinLimit = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -330,8 +399,10 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
     return d;                                     // base offset 0, swizzle none
 }
 
-// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N = 32, M = 128.
-constexpr uint32_t kTcIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
+// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N = 64, M = 128.
+// MMA N = 2 * kTcN: the activations' fp16 high parts are B rows 0..31, their low parts rows 32..63
+constexpr int kTcNM = 2 * kTcN;
+constexpr uint32_t kTcIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcNM >> 3) << 17) |
                               ((uint32_t)(kTcM >> 4) << 24);
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
@@ -354,18 +425,62 @@ __device__ __forceinline__ void store_half8(uint8_t* dst, const float (&v)[8]) {
     *(uint4*)dst = *(const uint4*)h;
 }
 
+// 32 consecutive fp32 accumulator columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Copies a thread's kTcVpt consecutive stage-`st` codewords (exact fp16 rows
+// of codebook st; the vectors' S code bytes each are in cw) to consecutive
+// core matrices along K of its weight-tile row.
+__device__ __forceinline__ void stage_run(const uint4* scb, const uint2 (&cw)[QMOE_RVQ_MAX_STAGES], int S, int st,
+                                          unsigned char* dst) {
+    const uint32_t words[6] = {cw[0].x, cw[0].y, cw[1].x, cw[1].y, cw[2].x, cw[2].y};
+#pragma unroll
+    for (int q = 0; q < kTcVpt; ++q) {
+        const int byte = q * S + st;
+        uint32_t w = words[0];
+#pragma unroll
+        for (int k = 1; k < 6; ++k)
+            if ((byte >> 2) == k) w = words[k];
+        const uint32_t code = (w >> (8 * (byte & 3))) & 255u;
+        *(uint4*)(dst + q * kTcLBO) = scb[256 * st + code];
+    }
+}
+
+// fp16 high part of 8 values, and the fp16 of what the high part leaves.
+__device__ __forceinline__ void store_hi_lo8(uint8_t* hi, uint8_t* lo, const float (&v)[8]) {
+    __half2 h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
+        const float2 hf = __half22float2(h[q]);
+        l[q] = __floats2half2_rn(v[2 * q] - hf.x, v[2 * q + 1] - hf.y);
+    }
+    *(uint4*)hi = *(const uint4*)h;
+    *(uint4*)lo = *(const uint4*)l;
+}
+
 __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint4* scb = (uint4*)smem;
-    uint8_t* abuf = smem + 2 * 256 * 16;                         // 2 x 32 KB
-    uint8_t* bbuf = abuf + 2 * kTcABytes;                         // 2 x 8 KB
-    uint64_t* bars = (uint64_t*)(bbuf + 2 * kTcBBytes);           // 2 mbarriers
+    uint8_t* abuf = smem + kTcCbBytes;                            // 2 x 32 KB
+    uint8_t* bbuf = abuf + 2 * kTcABytes;                         // 2 chunks x (high, low) x 8 KB
+    uint64_t* bars = (uint64_t*)(bbuf + 4 * kTcBBytes);           // 2 mbarriers
     uint32_t* tmem_slot = (uint32_t*)(bars + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const RvqDev& m = a.m;
 
-    for (int i = tid; i < 2 * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)m.cb + i);
+    for (int i = tid; i < m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)m.cb + i);
     if (tid == 0) {
         for (int b = 0; b < 2; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + b)) : "memory");
@@ -373,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kTcN)
+                     "r"(kTcNM)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -404,88 +519,102 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
         // per thread: A part (row, half of a chunk's 16 vectors), B part (token, two 8-wide K groups)
         const int rl = tid >> 1, part = tid & 1;
         const int arow = r0 + rl;
-        const uint8_t* ip = m.idx + (((size_t)job.matrix * m.rows + (arow < m.rows ? arow : 0)) * nv + part * kTcVpt) * 2;
+        const int S = stages_of(m, job.matrix);              // code bytes per vector (8-byte aligned runs of kTcVpt)
+        if (S == 0) continue;                                 // uniform over the block: skip the tile
+        const uint8_t* ip = codes_of(m, job.matrix) + ((size_t)(arow < m.rows ? arow : 0) * nv + part * kTcVpt) * S;
         const int bn = tid >> 3, bg = tid & 7;
         const int bslot = bn < job.n_tok ? (a.slots ? a.slots[job.slot_begin + bn] : job.slot_begin + bn) : -1;
         const float* bp = a.xr + (size_t)(bslot < 0 ? 0 : bslot) * m.cols + bg * 16;
         // the global loads of chunk kc + 1 are issued before chunk kc is decoded
-        uint4 pairs_n = arow < m.rows ? __ldg((const uint4*)ip) : make_uint4(0, 0, 0, 0);
+        // a thread's kTcVpt vectors of a chunk: 8 * S code bytes, as S 8-byte loads
+        uint2 cw_n[QMOE_RVQ_MAX_STAGES];
+#pragma unroll
+        for (int q = 0; q < QMOE_RVQ_MAX_STAGES; ++q)
+            cw_n[q] = arow < m.rows && q < S ? __ldg((const uint2*)ip + q) : make_uint2(0u, 0u);
         float4 xv_n[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) xv_n[q] = bslot >= 0 ? __ldg((const float4*)bp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int kc = 0; kc < nk; ++kc) {
-            const int b = kc & 1;
-            const uint4 pairs = pairs_n;
+        // Steps: for every chunk, one per stage.  A step copies the stage's exact fp16
+        // codewords into a weight tile (two tiles alternate) and issues its MMAs
+        // against the chunk's activations, split as fp16 high + low parts (staged
+        // at the chunk's first step, two chunk buffers alternate), so the product
+        // carries neither the fp16 rounding of a stage sum nor of x'.
+        int stp = 0;
+        for (int kc = 0; kc < nk && !timed_out; ++kc) {
+            uint2 cw[QMOE_RVQ_MAX_STAGES];
+#pragma unroll
+            for (int q = 0; q < QMOE_RVQ_MAX_STAGES; ++q) cw[q] = cw_n[q];
             float4 xv[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) xv[q] = xv_n[q];
             if (kc + 1 < nk) {
-                if (arow < m.rows) pairs_n = __ldg((const uint4*)(ip + (size_t)(kc + 1) * (kTcK / 8) * 2));
+                if (arow < m.rows) {
+                    const uint2* nx = (const uint2*)(ip + (size_t)(kc + 1) * (kTcK / 8) * S);
+#pragma unroll
+                    for (int q = 0; q < QMOE_RVQ_MAX_STAGES; ++q)
+                        if (q < S) cw_n[q] = __ldg(nx + q);
+                }
                 if (bslot >= 0) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) xv_n[q] = __ldg((const float4*)(bp + (size_t)(kc + 1) * kTcK) + q);
                 }
             }
-            if (commits[b] > waited[b]) {
-                // the MMAs that last read this buffer must be done before it is rewritten
-                if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
-                ++waited[b];
-            }
-            uint8_t* A = abuf + b * kTcABytes;
-            uint8_t* B = bbuf + b * kTcBBytes;
-            {
-                float w[8];
-                const uint32_t pw[4] = {pairs.x, pairs.y, pairs.z, pairs.w};
+            uint8_t* Bh = bbuf + (kc & 1) * 2 * kTcBBytes;           // N = 64 rows: high parts, then low
+            uint8_t* Bl = Bh + 4 * kTcSBO;
+            for (int st = 0; st < S; ++st, ++stp) {
+                const int b = stp & 1;
+                if (commits[b] > waited[b]) {
+                    // step stp - 2 (and so every earlier step: chunk kc - 2 included) has finished
+                    // reading this weight tile and the chunk buffer about to be rewritten
+                    if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
+                    ++waited[b];
+                }
+                uint8_t* A = abuf + b * kTcABytes;
+                unsigned char* arow_base = A + (rl >> 3) * kTcSBO + (rl & 7) * 16 + part * kTcVpt * kTcLBO;
+                if (arow >= m.rows) {
 #pragma unroll
-                for (int q = 0; q < kTcVpt; ++q) {
-                    const uint32_t pr = (pw[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-                    if (arow < m.rows) {
-                        decode8(scb[pr & 255u], scb[256 + (pr >> 8)], w);
-                    } else {
+                    for (int q = 0; q < kTcVpt; ++q) *(uint4*)(arow_base + q * kTcLBO) = make_uint4(0, 0, 0, 0);
+                } else {
+                    stage_run(scb, cw, S, st, arow_base);
+                }
+                if (st == 0) {
 #pragma unroll
-                        for (int z = 0; z < 8; ++z) w[z] = 0.0f;
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c8 = bg * 2 + h2;
+                        const float v[8] = {xv[2 * h2].x, xv[2 * h2].y, xv[2 * h2].z, xv[2 * h2].w,
+                                            xv[2 * h2 + 1].x, xv[2 * h2 + 1].y, xv[2 * h2 + 1].z, xv[2 * h2 + 1].w};
+                        const int o = (bn >> 3) * kTcSBO + c8 * kTcLBO + (bn & 7) * 16;
+                        store_hi_lo8(Bh + o, Bl + o, v);
                     }
-                    const int c8 = part * kTcVpt + q;
-                    store_half8(A + (rl >> 3) * kTcSBO + c8 * kTcLBO + (rl & 7) * 16, w);
                 }
-            }
-            {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (__syncthreads_or(timed_out)) {
+                    timed_out = true;
+                    break;
+                }
+                if (tid == 0) {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t a0 = smem_u32(A), b0 = smem_u32(Bh);
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c8 = bg * 2 + h2;
-                    const float v[8] = {xv[2 * h2].x, xv[2 * h2].y, xv[2 * h2].z, xv[2 * h2].w,
-                                        xv[2 * h2 + 1].x, xv[2 * h2 + 1].y, xv[2 * h2 + 1].z, xv[2 * h2 + 1].w};
-                    store_half8(B + (bn >> 3) * kTcSBO + c8 * kTcLBO + (bn & 7) * 16, v);
+                    for (int k = 0; k < kTcK / 16; ++k) {
+                        const uint32_t acc = (kc > 0 || st > 0 || k > 0) ? 1u : 0u;
+                        asm volatile(
+                            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+                            "l"(umma_desc(a0 + k * 2 * kTcLBO)), "l"(umma_desc(b0 + k * 2 * kTcLBO)), "r"(kTcIdesc),
+                            "r"(acc)
+                            : "memory");
+                    }
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     smem_u32(bars + b))
+                                 : "memory");
                 }
+                ++commits[b];
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            if (__syncthreads_or(timed_out)) {
-                timed_out = true;
-                break;
-            }
-            if (tid == 0) {
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
-#pragma unroll
-                for (int k = 0; k < kTcK / 16; ++k) {
-                    const uint64_t ad = umma_desc(a0 + k * 2 * kTcLBO);
-                    const uint64_t bd = umma_desc(b0 + k * 2 * kTcLBO);
-                    const uint32_t accum = (kc > 0 || k > 0) ? 1u : 0u;
-                    asm volatile(
-                        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
-                        "l"(ad), "l"(bd), "r"(kTcIdesc), "r"(accum)
-                        : "memory");
-                }
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 smem_u32(bars + b))
-                             : "memory");
-            }
-            ++commits[b];
         }
         // wait for every outstanding commit, oldest first
         for (int q = 0; q < 2; ++q) {
-            const int b = (nk + q) & 1;   // the buffer whose commit is older comes first
+            const int b = (stp + q) & 1;  // the buffer whose commit is older comes first
             while (commits[b] > waited[b]) {
                 if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
                 ++waited[b];
@@ -494,8 +623,9 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
         timed_out = __syncthreads_or(timed_out);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (warp < 4 && !timed_out) {
-            uint32_t r[32];
+            uint32_t r[32], rl2[32];
             const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+            tmem_ld32_at(taddr + kTcN, rl2);                      // the low parts' columns
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -513,7 +643,7 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
                 for (int n = 0; n < kTcN; ++n) {
                     if (n < job.n_tok) {
                         const int slot = a.slots ? a.slots[job.slot_begin + n] : job.slot_begin + n;
-                        a.out[(size_t)slot * m.rows + row] = s * __uint_as_float(r[n]);
+                        a.out[(size_t)slot * m.rows + row] = s * (__uint_as_float(r[n]) + __uint_as_float(rl2[n]));
                     }
                 }
             }
@@ -534,7 +664,7 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcN) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcNM) : "memory");
 }
 
 int launch_rvq_tc(RvqGemmArgs a, cudaStream_t st, long long tiles_hint) {
@@ -554,11 +684,23 @@ __global__ void rvq_decode_kernel(RvqDev m, float* __restrict__ out) {
     const size_t nv = (size_t)m.rows * (m.cols / 8);
     if (v >= nv) return;
     const int r = (int)(v / (m.cols / 8));
-    const uint32_t i1 = m.idx[2 * v], i2 = m.idx[2 * v + 1];
-    const uint4 c1 = __ldg((const uint4*)m.cb + i1);
-    const uint4 c2 = __ldg((const uint4*)m.cb + 256 + i2);
+    const int S = stages_of(m, 0);
+    const uint8_t* ip = codes_of(m, 0) + v * S;
+    const uint4* cb = (const uint4*)m.cb;
     float w[8];
-    decode8(c1, c2, w);
+    if (S == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = 0.0f;
+    } else if (S == 1) {
+        const uint32_t code[1] = {ip[0]};
+        decode_vec<1>(cb, code, w);
+    } else if (S == 2) {
+        const uint32_t code[2] = {ip[0], ip[1]};
+        decode_vec<2>(cb, code, w);
+    } else {
+        const uint32_t code[3] = {ip[0], ip[1], ip[2]};
+        decode_vec<3>(cb, code, w);
+    }
     const float s = f16_to_f32(m.scale[r]);
     float* o = out + v * 8;
 #pragma unroll
@@ -567,14 +709,18 @@ __global__ void rvq_decode_kernel(RvqDev m, float* __restrict__ out) {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-int launch_rvq_gemm(RvqGemmArgs a, cudaStream_t st) {
+// jobs_hint: an upper bound on the launch's jobs; the row tiles shrink (down to 16 rows) until there
+// are about two tiles per SM.
+int launch_rvq_gemm(RvqGemmArgs a, cudaStream_t st, long long jobs_hint) {
     const int sms = qmoe::sm_count();
-    const size_t smem = 2 * 256 * 16 + (size_t)a.m.cols * a.nt_max * 4;
+    const size_t smem = (size_t)a.m.n_st * 256 * 16 + (size_t)a.m.cols * a.nt_max * 4;
     int rc = qmoe::cuda_check(
         cudaFuncSetAttribute(rvq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem), "rvq attr");
     if (rc) return rc;
-    a.rows_per_tile = 16;
-    a.row_tiles = (a.m.rows + 15) / 16;
+    int rpt = std::min(a.m.rows, 128);
+    while (rpt > 16 && std::max(1LL, jobs_hint) * ((a.m.rows + rpt - 1) / rpt) < 2LL * sms) rpt >>= 1;
+    a.rows_per_tile = rpt;
+    a.row_tiles = (a.m.rows + a.rows_per_tile - 1) / a.rows_per_tile;
     rvq_gemm_kernel<<<sms * 2, kRvqThreads, smem, st>>>(a);
     return qmoe::launch_check("rvq_gemm_kernel");
 }
@@ -584,8 +730,11 @@ int nt_for(int cols) {
     return cols * 8 * 4 <= 65536 ? 8 : cols * 4 * 4 <= 65536 ? 4 : 1;
 }
 
-// Tensor-core path: batches of 16+ activation rows and K a multiple of the 128-wide chunk.
-bool use_tc(long long rows_of_x, int cols) { return rows_of_x >= 16 && cols % kTcK == 0; }
+// Tensor-core path: a launch with at least kTcMinTokens activation rows, K a multiple of the
+// 128-wide chunk.  An M128 x K16 MMA costs about 83 cycles whatever N <= 64 is, so the tensor
+// path's cost is per weight (one MMA per stage and K16 step), not per token.
+constexpr int kTcMinTokens = 16;
+bool use_tc(long long rows_of_x, int cols) { return rows_of_x >= kTcMinTokens && cols % kTcK == 0; }
 
 float inv_sqrt(int n) { return (float)(1.0 / std::sqrt((double)n)); }
 
@@ -660,7 +809,7 @@ extern "C" int rvq_expert_matmul(const rvq_matrix_set* mat, const void* x_bf16, 
     a.nt_max = nt_for(cols);
     a.out = yr;
     if (use_tc(T, cols)) rc = launch_rvq_tc(a, st, (long long)((T + kTcN - 1) / kTcN) * ((rows + kTcM - 1) / kTcM));
-    else rc = launch_rvq_gemm(a, st);
+    else rc = launch_rvq_gemm(a, st, (T + a.nt_max - 1) / a.nt_max);
     if (rc) return rc;
     return launch_out_transform(yr, nullptr, mat->sign_out, nullptr, T, 1, rows, y, y_is_f32 ? 1 : 0, st);
 }
@@ -734,10 +883,13 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     if (ws_bytes < w.bytes) return fail(QMOE_ECAPACITY, "rvq_moe_layer: workspace too small");
     cudaStream_t st = (cudaStream_t)stream;
     const int slots = T * k;
+    // with at least kTcMinTokens slots every expert takes the tensor-core kernel (jobs of kTcN
+    // tokens): its cost is per weight, whatever the expert's token count; fewer slots take the
+    // CUDA-core kernel
     const bool tc = use_tc(slots, d_model) && use_tc(slots, d_ff);
     const int nt_a = tc ? kTcN : nt_for(d_model), nt_b = tc ? kTcN : nt_for(d_ff);
     auto gemm = [&](RvqGemmArgs& ga, int rows) {
-        return tc ? launch_rvq_tc(ga, st, (long long)slots * ((rows + kTcM - 1) / kTcM)) : launch_rvq_gemm(ga, st);
+        return tc ? launch_rvq_tc(ga, st, (long long)slots * ((rows + kTcM - 1) / kTcM)) : launch_rvq_gemm(ga, st, slots);
     };
     qmoe::phase_event(0, st);
     int rc = qmoe::launch_plan(ids, slots, E, nt_a, nt_b, w.counts, w.offsets, w.perm, w.jobs_a, w.jobs_b, w.n_jobs, st);

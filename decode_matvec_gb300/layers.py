@@ -101,20 +101,23 @@ class DictLayer:
 
 
 def pack_rvq_set(count: int, rows: int, cols: int, codebooks_f16: np.ndarray, weight_fn, sign_fn,
-                 threads: int | None = None, device="cuda") -> RvqMatrixSet:
-    """Encode `count` RVQ matrices: weight_fn(e) -> float64 [rows, cols], sign_fn(e) -> (sign_out, sign_in)."""
-    idx = np.zeros((count, rows, cols // 8, 2), dtype=np.uint8)
+                 threads: int | None = None, device="cuda", stages=None) -> RvqMatrixSet:
+    """Encode `count` RVQ matrices: weight_fn(e) -> float64 [rows, cols], sign_fn(e) -> (sign_out, sign_in).
+    stages: None (two stages each, two codebooks given) or per-matrix stage counts (1 .. codebooks given)."""
     scales = np.zeros((count, rows), dtype=np.uint16)
     so = np.zeros((count, rows), dtype=np.int8)
     si = np.zeros((count, cols), dtype=np.int8)
+    cb = np.ascontiguousarray(codebooks_f16, dtype=np.uint16)
+    per = [None] * count
 
     def work(e):
         w = weight_fn(e)
         s_out, s_in = sign_fn(e)
-        idx[e], scales[e] = rvq_pack(w, s_out, s_in, codebooks_f16)
+        per[e], scales[e] = rvq_pack(w, s_out, s_in, cb, 2 if stages is None else int(stages[e]))
         so[e], si[e] = s_out, s_in
 
     with cf.ThreadPoolExecutor(max_workers=_threads(threads)) as ex:
         list(ex.map(work, range(count)))
-    return RvqMatrixSet.from_host(idx, codebooks_f16, scales.reshape(-1), so.reshape(-1), si.reshape(-1), count,
-                                  rows, cols, device=device)
+    idx = np.stack(per) if stages is None else per
+    return RvqMatrixSet.from_host(idx, cb if stages is not None else cb[:2], scales.reshape(-1), so.reshape(-1),
+                                  si.reshape(-1), count, rows, cols, device=device)

@@ -63,6 +63,8 @@ typedef enum {
 #define QMOE_COMPACT_BYTES (3 * QMOE_DICT_ENTRIES)
 #define QMOE_RVQ_DIM 8
 #define QMOE_RVQ_CODES 256
+/* most residual stages an RVQ code may have */
+#define QMOE_RVQ_MAX_STAGES 3
 
 /* ======================================================================
  * Host-side codec (dictionary format)
@@ -284,16 +286,26 @@ int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_set* wi,
  * ====================================================================== */
 
 /*
- * `count` RVQ-coded matrices of the same shape.  For matrix e:
- *  idx       device uint8 [count][rows][cols/8][2]: stage-1 and stage-2
- *            codebook indices of each 8-weight vector of the rotated weight;
- *  codebooks device fp16 bits [2][256][8] shared by the whole set;
+ * `count` RVQ-coded matrices of the same shape.  Matrix e has S_e residual
+ * stages (2 for every matrix unless `stages` is given):
+ *  idx       device uint8: matrix e's codes start at idx + idx_base[e]
+ *            (idx_base NULL: at e*rows*(cols/8)*2) and are [rows][cols/8][S_e]
+ *            codebook indices of each 8-weight vector of the rotated weight,
+ *            stage 1 first;
+ *  codebooks device fp16 bits [n_stages][256][8] shared by the whole set;
  *  scale_f16 device [count][rows] fp16 per-row scales;
- *  sign_out  device int8 [count][rows] (+1/-1), sign_in [count][cols].
- * rows and cols are powers of two (2 .. 8192), cols a multiple of 8.
- * Decoded rotated weight: W'[r][8v+j] = fp32(s_r) * (fp32(C1[i1][j]) +
- * fp32(C2[i2][j])); layer output y = D_out H_rows (W' (H_cols D_in x)) with
- * H the normalised Walsh-Hadamard matrix.
+ *  sign_out  device int8 [count][rows] (+1/-1), sign_in [count][cols];
+ *  stages    device uint8 [count], each in 1 .. n_stages, or NULL (all 2);
+ *  idx_base  device uint64 [count] byte offsets, or NULL;
+ *  n_stages  codebooks in the set (0 means 2), at most QMOE_RVQ_MAX_STAGES.
+ * Frequency-conditioned allocation ("Quantization as Cache Amplification",
+ * Frequency-Conditioned Bit Allocation) gives popular experts more stages;
+ * see rvq_stage_allocation.  rows and cols are powers of two (2 .. 8192),
+ * cols a multiple of 8.  Decoded rotated weight: W'[r][8v+j] =
+ * fp32(s_r) * (((fp32(C1[i1][j]) + fp32(C2[i2][j])) + fp32(C3[i3][j])) ...),
+ * the adds left to right over the matrix's stages; layer output
+ * y = D_out H_rows (W' (H_cols D_in x)) with H the normalised Walsh-Hadamard
+ * matrix.  Zero-initialising the last three fields gives the two-stage set.
  */
 typedef struct {
     const uint8_t* idx;
@@ -302,6 +314,9 @@ typedef struct {
     const int8_t* sign_out;
     const int8_t* sign_in;
     int count, rows, cols;
+    const uint8_t* stages;
+    const uint64_t* idx_base;
+    int n_stages;
 } rvq_matrix_set;
 
 /* Workspace bytes for rvq_expert_matmul. */
@@ -354,6 +369,29 @@ int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* up,
 int rvq_pack(const double* w, int rows, int cols, const int8_t* sign_out,
              const int8_t* sign_in, const uint16_t* codebooks, uint8_t* idx,
              uint16_t* scale_f16);
+
+/*
+ * rvq_pack with n_stages residual stages (1 .. QMOE_RVQ_MAX_STAGES): stage s
+ * takes the codeword of codebooks[s] nearest to what stages 1 .. s-1 leave
+ * of u (float64 residuals).  codebooks host fp16 bits [n_stages][256][8];
+ * idx host out uint8 [rows][cols/8][n_stages].  rvq_pack is n_stages = 2.
+ */
+int rvq_pack_stages(const double* w, int rows, int cols, const int8_t* sign_out,
+                    const int8_t* sign_in, const uint16_t* codebooks, int n_stages,
+                    uint8_t* idx, uint16_t* scale_f16);
+
+/*
+ * Stages per expert for an average of s_bar ("Quantization as Cache
+ * Amplification", Frequency-Conditioned Bit Allocation, rank-based form):
+ * the floor(E/3) most popular experts get s_bar + 1 stages, the floor(E/3)
+ * least popular s_bar - 1, the others s_bar, so the mean rate is s_bar.
+ * Equal popularity ranks the lower expert id as more popular.
+ *  popularity host float64 [E] (any positive weights, e.g. activation
+ *             frequencies);  stages host out uint8 [E].
+ * Errors: EINVAL (NULL, E < 1, s_bar - 1 or s_bar + 1 outside
+ * 1 .. QMOE_RVQ_MAX_STAGES when E >= 3).
+ */
+int rvq_stage_allocation(const double* popularity, int E, int s_bar, uint8_t* stages);
 
 /* ======================================================================
  * Status and test exports

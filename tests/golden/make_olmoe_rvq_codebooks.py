@@ -1,11 +1,13 @@
-"""Writes olmoe_rvq_codebooks.npy: the OLMoE-shaped layer's two fp16 RVQ codebooks.
+"""Writes olmoe_rvq_codebooks.npy and olmoe_rvq_codebooks3.npy: the OLMoE-shaped layer's fp16 RVQ
+codebook sets with two and with three stages (the first two stages of both are the same).
 
 Calls only the oracle (and the seeded generators).  One codebook pair serves the
 whole layer ("a single global codebook", Quantization as Cache Amplification,
 section "Codec"): k-means (256 centroids, 25 Lloyd iterations or stable
 assignments, lowest-index ties, empty clusters keep their centroid) on a seeded
 pool of 2**17 8-dim vectors of the row-normalised rotated weights drawn evenly
-from all 64 experts x 3 matrices; stage 2 is fit on the stage-1 residual.
+from all 64 experts x 3 matrices; stage s is fit on what stages 1 .. s-1 leave.  The three-stage set
+serves the frequency-conditioned layer, whose most popular experts use a third stage.
 
 Run from the repository root:  python tests/golden/make_olmoe_rvq_codebooks.py
 """
@@ -37,10 +39,12 @@ def main():
             u = R.normalised_vectors(wr, R.row_scale_f16(wr), cfg.vec_dim)
             pool.append(u[np.sort(rng.choice(u.shape[0], size=per, replace=False))])
     pool = np.concatenate(pool)
-    cb = R.fit_codebooks(pool, k=cfg.codebook_size, iters=25, seed=cfg.seed)
-    out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "olmoe_rvq_codebooks.npy")
-    np.save(out, cb.astype(np.float16))
-    print(f"wrote {out}: pool {pool.shape}, codebooks {cb.shape}")
+    cb = R.fit_codebooks(pool, k=cfg.codebook_size, iters=25, seed=cfg.seed, stages=3)
+    here = os.path.dirname(os.path.abspath(__file__))
+    for name, c in (("olmoe_rvq_codebooks.npy", cb[:2]), ("olmoe_rvq_codebooks3.npy", cb)):
+        out = os.path.join(here, name)
+        np.save(out, c.astype(np.float16))
+        print(f"wrote {out}: pool {pool.shape}, codebooks {c.shape}")
 
 
 if __name__ == "__main__":

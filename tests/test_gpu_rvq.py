@@ -115,3 +115,95 @@ def test_rvq_moe_layer_parity(dev, E, d, f, T, k):
 
     ref = M.moe_layer(synth.bf16_to_f64(xb), rid, rg, expert, d)
     assert P.normwise_rel_err(y.cpu().numpy(), ref) < TOL
+
+
+# ------------------------------------------------------ per-matrix stage counts
+def _matrix_st(seed, e, m, rows, cols, cb, stages):
+    w = synth.rvq_weight(seed, e, m, rows, cols)
+    so, si = synth.rvq_signs(seed, e, m, rows, cols)
+    wr = R.rotate_weight(w, so, si)
+    idx, sc = R.encode(wr, cb, stages=stages)
+    return dict(w=w, so=so, si=si, idx=idx, scale=sc, cb=cb.astype(np.float16).view(np.uint16))
+
+
+def _set_st(mats, rows, cols):
+    return Q.RvqMatrixSet.from_host([m["idx"] for m in mats], mats[0]["cb"],
+                                    np.concatenate([m["scale"] for m in mats]),
+                                    np.concatenate([m["so"] for m in mats]), np.concatenate([m["si"] for m in mats]),
+                                    len(mats), rows, cols)
+
+
+def _cb3(seed, rows, cols):
+    w = synth.rvq_weight(seed, 0, 0, rows, cols)
+    so, si = synth.rvq_signs(seed, 0, 0, rows, cols)
+    wr = R.rotate_weight(w, so, si)
+    return R.fit_codebooks(R.normalised_vectors(wr, R.row_scale_f16(wr), 8), k=256, iters=3, seed=seed, stages=3)
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_rvq_decode_bit_exact_any_stage_count(dev, stages):
+    rows, cols = 128, 256
+    cb = _cb3(8, rows, cols)
+    mt = _matrix_st(8, 1, 0, rows, cols, cb, stages)
+    s = _set_st([mt], rows, cols)
+    w = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    Q.rvq_decode_dense(s, w)
+    assert Q.qmoe_check_status() == Q.QMOE_OK
+    assert np.array_equal(w.cpu().numpy(), R.decode(mt["idx"], mt["cb"], mt["scale"]))
+
+
+@pytest.mark.parametrize("stages,T", [(1, 1), (3, 1), (1, 32), (3, 32), (3, 5)])
+def test_rvq_expert_matmul_any_stage_count(dev, stages, T):
+    rows, cols = 256, 512
+    cb = _cb3(9, rows, cols)
+    mt = _matrix_st(9, 2, 0, rows, cols, cb, stages)
+    s = _set_st([mt], rows, cols)
+    xb = synth.activations_bf16(9, T, cols)
+    y = torch.empty((T, rows), dtype=torch.float32, device=dev)
+    ws = torch.empty(Q.rvq_expert_matmul_ws_size(rows, cols, T), dtype=torch.uint8, device=dev)
+    Q.rvq_expert_matmul(s, bf16_tensor(xb), y, ws)
+    assert Q.qmoe_check_status() == Q.QMOE_OK
+    ref = R.linear(synth.bf16_to_f64(xb), R.decode(mt["idx"], mt["cb"], mt["scale"]), mt["so"], mt["si"])
+    assert P.normwise_rel_err(y.cpu().numpy(), ref) < TOL
+
+
+@pytest.mark.parametrize("E,d,f,T,k", [(9, 256, 128, 24, 4), (6, 128, 256, 3, 2), (4, 256, 128, 64, 2)])
+def test_rvq_moe_layer_frequency_conditioned_parity(dev, E, d, f, T, k):
+    """Experts with 3 / 2 / 1 stages by popularity thirds (the layer's fixed Zipf popularity)."""
+    seed = 41
+    pop = synth.zipf_popularity(seed, E, 0.9)
+    st = Q.rvq_stage_allocation(pop, 2)
+    assert np.array_equal(st, R.stage_allocation(pop, 2))
+    cb = _cb3(seed, f, d)
+    gate = [_matrix_st(seed, e, synth.GATE, f, d, cb, int(st[e])) for e in range(E)]
+    up = [_matrix_st(seed, e, synth.UP, f, d, cb, int(st[e])) for e in range(E)]
+    down = [_matrix_st(seed, e, synth.DOWN, d, f, cb, int(st[e])) for e in range(E)]
+    sg, su, sd = _set_st(gate, f, d), _set_st(up, f, d), _set_st(down, d, f)
+    lg = synth.zipf_layer_logits(seed, T, E, 0.9)
+    xb = synth.activations_bf16(seed, T, d)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+    Q.qmoe_route(torch.from_numpy(lg).to(dev), k, ids, gates)
+    ws = torch.empty(Q.rvq_moe_layer_ws_size(E, d, f, T, k), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    Q.rvq_moe_layer(sg, su, sd, bf16_tensor(xb), ids, gates, y, ws)
+    assert Q.qmoe_check_status() == Q.QMOE_OK
+    rid, rg = M.route(lg, k)
+
+    def expert(e, xs):
+        trip = [(R.decode(m["idx"], m["cb"], m["scale"]), m["so"], m["si"]) for m in (gate[e], up[e], down[e])]
+        return R.swiglu_expert(xs, *trip)
+
+    ref = M.moe_layer(synth.bf16_to_f64(xb), rid, rg, expert, d)
+    assert P.normwise_rel_err(y.cpu().numpy(), ref) < TOL
+
+
+def test_rvq_bad_stage_count_reported(dev):
+    rows, cols = 64, 128
+    cb = _cb3(10, rows, cols)
+    mt = _matrix_st(10, 0, 0, rows, cols, cb, 2)
+    s = _set_st([mt], rows, cols)
+    s.stages.fill_(5)                       # more stages than the set's three codebooks
+    w = torch.empty((rows, cols), dtype=torch.float32, device=dev)
+    Q.rvq_decode_dense(s, w)
+    assert Q.qmoe_check_status() == Q.QMOE_EFORMAT

@@ -135,3 +135,36 @@ def test_native_ternary_generator_matches_python():
         out = np.zeros((n, cols), np.int8)
         lib.synth_ternary_rows(seed, e, m, cols, synth.zero_threshold(p0), r0, n, out.ctypes.data)
         assert np.array_equal(out, synth.ternary_rows(seed, e, m, cols, p0, r0, n))
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_rvq_pack_stages_matches_oracle(stages):
+    rows, cols = 32, 128
+    w = synth.rvq_weight(4, 2, 0, rows, cols)
+    so, si = synth.rvq_signs(4, 2, 0, rows, cols)
+    wr = R.rotate_weight(w, so, si)
+    u = R.normalised_vectors(wr, R.row_scale_f16(wr), 8)
+    cb = R.fit_codebooks(u, k=256, iters=3, seed=5, stages=3)
+    idx, sc = Q.rvq_pack(w, so, si, cb.astype(np.float16).view(np.uint16), stages)
+    ridx, rsc = R.encode(wr, cb, stages=stages)
+    assert idx.shape == (rows, cols // 8, stages)
+    assert np.array_equal(sc, rsc) and np.array_equal(idx, ridx)
+
+
+def test_rvq_stage_allocation_matches_oracle():
+    for E, seed in ((64, 4), (7, 1), (2, 3), (30, 9)):
+        pop = synth.zipf_popularity(seed, E, 0.9)
+        assert np.array_equal(Q.rvq_stage_allocation(pop, 2), R.stage_allocation(pop, 2))
+    ties = np.array([1.0, 2.0, 2.0, 1.0, 2.0, 0.5])
+    assert np.array_equal(Q.rvq_stage_allocation(ties, 2), R.stage_allocation(ties, 2))
+    with pytest.raises(Q.QmoeError):
+        Q.rvq_stage_allocation(np.ones(6), 3)          # s_bar + 1 = 4 stages is beyond the maximum
+
+
+def test_three_stage_codebook_fixture_extends_the_two_stage_one():
+    """The committed codebook sets: the first two stages of the three-stage set are the two-stage set."""
+    golden = os.path.join(ROOT, "tests", "golden")
+    cb2 = np.load(os.path.join(golden, "olmoe_rvq_codebooks.npy"))
+    cb3 = np.load(os.path.join(golden, "olmoe_rvq_codebooks3.npy"))
+    assert cb2.shape == (2, 256, 8) and cb3.shape == (3, 256, 8)
+    assert np.array_equal(cb3[:2].view(np.uint16), cb2.view(np.uint16))
