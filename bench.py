@@ -383,17 +383,27 @@ def _dict_layer_row(layer, cfg, T, device, peak, note=""):
             "stream_bytes": sb, "stream_gbs": sb / t / 1e9, "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak}
 
 
-def _rvq_rows(device, peak):
+def _rvq_rows(device, peak, cfg=None):
+    """The OLMoE-shaped RVQ layer at T = 1 and 32.  With cfg.freq_stages, expert e's matrices have
+    rvq_stage_allocation(popularity)[e] stages (3 / 2 / 1 by popularity thirds, mean 2 bits per
+    weight) and the router uses the layer's fixed popularity."""
     import torch
     import decode_matvec_gb300 as Q
     from decode_matvec_gb300.layers import pack_rvq_set
-    cfg = synth.OLMOE_RVQ
-    cb = np.load(os.path.join(ROOT, "tests", "golden", "olmoe_rvq_codebooks.npy")).view(np.uint16)
+    cfg = cfg or synth.OLMOE_RVQ
+    golden = os.path.join(ROOT, "tests", "golden")
+    if cfg.freq_stages:
+        cb = np.load(os.path.join(golden, "olmoe_rvq_codebooks3.npy")).view(np.uint16)
+        stages = Q.rvq_stage_allocation(synth.zipf_popularity(cfg.seed, cfg.E, cfg.zipf_s), cfg.stages)
+    else:
+        cb = np.load(os.path.join(golden, "olmoe_rvq_codebooks.npy")).view(np.uint16)
+        stages = None
     sets = []
     for m in (synth.GATE, synth.UP, synth.DOWN):
         rows, cols = synth.rvq_matrix_shape(cfg, m)
         sets.append(pack_rvq_set(cfg.E, rows, cols, cb, lambda e, m=m, r=rows, c=cols: synth.rvq_weight(cfg.seed, e, m, r, c),
-                                 lambda e, m=m, r=rows, c=cols: synth.rvq_signs(cfg.seed, e, m, r, c), device=device))
+                                 lambda e, m=m, r=rows, c=cols: synth.rvq_signs(cfg.seed, e, m, r, c), device=device,
+                                 stages=stages))
     out = []
     for T in cfg.tokens:
         lg = torch.from_numpy(synth.layer_logits(cfg, T)).to(device)
@@ -409,11 +419,15 @@ def _rvq_rows(device, peak):
             Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws, y_is_f32=False)
         t = _time_calls(step)
         touched = np.unique(ids.cpu().numpy().reshape(-1))
-        per_expert = sum(r * (c // 8) * 2 + r * 2 + r + c for r, c in
-                         (synth.rvq_matrix_shape(cfg, m) for m in (synth.GATE, synth.UP, synth.DOWN)))
-        sb = len(touched) * per_expert + 2 * 256 * 8 * 2
+        sb = 2 * 256 * 8 * cb.shape[0]
+        for e in touched:
+            s_e = 2 if stages is None else int(stages[e])
+            sb += sum(r * (c // 8) * s_e + r * 2 + r + c for r, c in
+                      (synth.rvq_matrix_shape(cfg, m) for m in (synth.GATE, synth.UP, synth.DOWN)))
+        label = "2-stage RVQ d=8" if stages is None else \
+            "RVQ d=8, 3/2/1 stages by popularity thirds (2 bits mean)"
         out.append({"workload": f"{cfg.name} SwiGLU MoE layer (E={cfg.E}, d={cfg.d_model}, f={cfg.d_ff}, top-8, "
-                                f"2-stage RVQ d=8), T={T}" + (" (tcgen05 path)" if T * cfg.top_k >= 16 else ""),
+                                f"{label}), T={T}" + (" (tcgen05 path)" if T * cfg.top_k >= 16 else ""),
                     "tokens_per_s": T / t, "ms_per_call": t * 1e3, "touched_experts": int(len(touched)),
                     "stream_bytes": int(sb), "stream_gbs": sb / t / 1e9,
                     "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak})
@@ -445,6 +459,7 @@ def extra_rows(layer, device, peak):
             return r
         guarded(one)
     guarded(lambda: _rvq_rows(device, peak))
+    guarded(lambda: _rvq_rows(device, peak, synth.OLMOE_RVQ_FREQ))
 
     def linear():
         lc = synth.LINEAR_1024x4096
@@ -656,7 +671,9 @@ def main():
     torch.cuda.set_device(device)
     if args.rvq_rows:
         if rank == 0:
-            print(json.dumps({"workload": "olmoe-rvq rows (profiling case)", "rows": _rvq_rows(device, hbm_peak()[0])}))
+            print(json.dumps({"workload": "olmoe-rvq rows (profiling case)",
+                              "rows": _rvq_rows(device, hbm_peak()[0]) + _rvq_rows(device, hbm_peak()[0],
+                                                                                 synth.OLMOE_RVQ_FREQ)}))
         return 0
     t_setup = time.time()
     layer = build_dict_layer(CFG, device)
