@@ -443,15 +443,14 @@ __device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&r)[32]) 
 // core matrices along K of its weight-tile row.
 __device__ __forceinline__ void stage_run(const uint4* scb, const uint2 (&cw)[QMOE_RVQ_MAX_STAGES], int S, int st,
                                           unsigned char* dst) {
-    const uint32_t words[6] = {cw[0].x, cw[0].y, cw[1].x, cw[1].y, cw[2].x, cw[2].y};
+    const uint64_t c0 = ((uint64_t)cw[0].y << 32) | cw[0].x;
+    const uint64_t c1 = ((uint64_t)cw[1].y << 32) | cw[1].x;
+    const uint64_t c2 = ((uint64_t)cw[2].y << 32) | cw[2].x;
 #pragma unroll
     for (int q = 0; q < kTcVpt; ++q) {
-        const int byte = q * S + st;
-        uint32_t w = words[0];
-#pragma unroll
-        for (int k = 1; k < 6; ++k)
-            if ((byte >> 2) == k) w = words[k];
-        const uint32_t code = (w >> (8 * (byte & 3))) & 255u;
+        const int byte = q * S + st;                      // < 8 * QMOE_RVQ_MAX_STAGES
+        const uint64_t c = byte < 8 ? c0 : byte < 16 ? c1 : c2;
+        const uint32_t code = (uint32_t)(c >> (8 * (byte & 7))) & 255u;
         *(uint4*)(dst + q * kTcLBO) = scb[256 * st + code];
     }
 }
@@ -497,8 +496,9 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    uint32_t commits[2] = {0, 0};     // commits issued per buffer (tracked identically by every thread)
-    uint32_t waited[2] = {0, 0};
+    // weight-tile steps issued by this block (step j uses tile and barrier j & 1, its commit
+    // completes barrier phase j >> 1); every step up to done - 1 is known to have completed
+    uint32_t gs = 0, done = 0;
     bool timed_out = false;
     const int nv = m.cols / 8;
     const int nk = m.cols / kTcK;
@@ -539,7 +539,6 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
         // against the chunk's activations, split as fp16 high + low parts (staged
         // at the chunk's first step, two chunk buffers alternate), so the product
         // carries neither the fp16 rounding of a stage sum nor of x'.
-        int stp = 0;
         for (int kc = 0; kc < nk && !timed_out; ++kc) {
             uint2 cw[QMOE_RVQ_MAX_STAGES];
 #pragma unroll
@@ -561,13 +560,13 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
             }
             uint8_t* Bh = bbuf + (kc & 1) * 2 * kTcBBytes;           // N = 64 rows: high parts, then low
             uint8_t* Bl = Bh + 4 * kTcSBO;
-            for (int st = 0; st < S; ++st, ++stp) {
-                const int b = stp & 1;
-                if (commits[b] > waited[b]) {
-                    // step stp - 2 (and so every earlier step: chunk kc - 2 included) has finished
+            for (int st = 0; st < S; ++st) {
+                const int b = gs & 1u;
+                if (gs >= 2 && done + 1 < gs) {
+                    // step gs - 2 (and so every earlier step: chunk kc - 2 included) has finished
                     // reading this weight tile and the chunk buffer about to be rewritten
-                    if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
-                    ++waited[b];
+                    if (!mbar_wait(smem_u32(bars + b), ((gs - 2) >> 1) & 1u)) timed_out = true;
+                    done = gs - 1;
                 }
                 uint8_t* A = abuf + b * kTcABytes;
                 unsigned char* arow_base = A + (rl >> 3) * kTcSBO + (rl & 7) * 16 + part * kTcVpt * kTcLBO;
@@ -609,17 +608,13 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
                                      smem_u32(bars + b))
                                  : "memory");
                 }
-                ++commits[b];
+                ++gs;
             }
         }
-        // wait for every outstanding commit, oldest first
-        for (int q = 0; q < 2; ++q) {
-            const int b = (stp + q) & 1;  // the buffer whose commit is older comes first
-            while (commits[b] > waited[b]) {
-                if (!mbar_wait(smem_u32(bars + b), waited[b] & 1u)) timed_out = true;
-                ++waited[b];
-            }
-        }
+        // wait for the outstanding steps (the last two at most), oldest first
+        for (uint32_t j = (done + 2 > gs ? done : gs - 2); j < gs; ++j)
+            if (!mbar_wait(smem_u32(bars + (j & 1u)), (j >> 1) & 1u)) timed_out = true;
+        done = gs;
         timed_out = __syncthreads_or(timed_out);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (warp < 4 && !timed_out) {
@@ -653,11 +648,8 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
     }
     if (timed_out) {
         // give the tensor core one more bounded chance to finish before the memory is freed
-        for (int b = 0; b < 2; ++b)
-            while (commits[b] > waited[b]) {
-                mbar_wait(smem_u32(bars + b), waited[b] & 1u);
-                ++waited[b];
-            }
+        for (uint32_t j = (done + 2 > gs ? done : gs - 2); j < gs; ++j)
+            mbar_wait(smem_u32(bars + (j & 1u)), (j >> 1) & 1u);
         if (tid == 0) atomicCAS(&g_rvq_error, 0, QMOE_ETIMEOUT);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
