@@ -418,13 +418,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void store_half8(uint8_t* dst, const float (&v)[8]) {
-    __half2 h[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) h[q] = __floats2half2_rn(v[2 * q], v[2 * q + 1]);
-    *(uint4*)dst = *(const uint4*)h;
-}
-
 // 32 consecutive fp32 accumulator columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tmem_ld32_at(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
