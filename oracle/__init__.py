@@ -10,6 +10,8 @@ Plain, slow, obviously-correct float64 restatements of what the pages define:
 * ``moe``        -- router, expert bucketing and the MoE feed-forward layer.
 * ``rvq``        -- randomized Hadamard transform, k-means residual VQ and the
   transform-aware product.
+* ``e8p``        -- the E8P structured lattice codebook (16-bit code words over a
+  1 KiB base table), its brute-force nearest-codeword encoder and decoder.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  It shares no code with the CUDA path
