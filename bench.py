@@ -389,10 +389,14 @@ def _rvq_rows(device, peak, cfg=None):
     weight) and the router uses the layer's fixed popularity."""
     import torch
     import decode_matvec_gb300 as Q
-    from decode_matvec_gb300.layers import pack_rvq_set
+    from decode_matvec_gb300.layers import pack_e8p_set, pack_rvq_set
     cfg = cfg or synth.OLMOE_RVQ
     golden = os.path.join(ROOT, "tests", "golden")
-    if cfg.freq_stages:
+    e8p = cfg.vq == "e8p"
+    if e8p:
+        cb = np.zeros((0, 256, 8), dtype=np.uint16)
+        stages = None
+    elif cfg.freq_stages:
         cb = np.load(os.path.join(golden, "olmoe_rvq_codebooks3.npy")).view(np.uint16)
         stages = Q.rvq_stage_allocation(synth.zipf_popularity(cfg.seed, cfg.E, cfg.zipf_s), cfg.stages)
     else:
@@ -401,9 +405,10 @@ def _rvq_rows(device, peak, cfg=None):
     sets = []
     for m in (synth.GATE, synth.UP, synth.DOWN):
         rows, cols = synth.rvq_matrix_shape(cfg, m)
-        sets.append(pack_rvq_set(cfg.E, rows, cols, cb, lambda e, m=m, r=rows, c=cols: synth.rvq_weight(cfg.seed, e, m, r, c),
-                                 lambda e, m=m, r=rows, c=cols: synth.rvq_signs(cfg.seed, e, m, r, c), device=device,
-                                 stages=stages))
+        wfn = lambda e, m=m, r=rows, c=cols: synth.rvq_weight(cfg.seed, e, m, r, c)   # noqa: E731
+        sfn = lambda e, m=m, r=rows, c=cols: synth.rvq_signs(cfg.seed, e, m, r, c)    # noqa: E731
+        sets.append(pack_e8p_set(cfg.E, rows, cols, wfn, sfn, device=device) if e8p else
+                    pack_rvq_set(cfg.E, rows, cols, cb, wfn, sfn, device=device, stages=stages))
     out = []
     for T in cfg.tokens:
         lg = torch.from_numpy(synth.layer_logits(cfg, T)).to(device)
@@ -419,12 +424,12 @@ def _rvq_rows(device, peak, cfg=None):
             Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws, y_is_f32=False)
         t = _time_calls(step)
         touched = np.unique(ids.cpu().numpy().reshape(-1))
-        sb = 2 * 256 * 8 * cb.shape[0]
+        sb = 1024 if e8p else 2 * 256 * 8 * cb.shape[0]
         for e in touched:
             s_e = 2 if stages is None else int(stages[e])
             sb += sum(r * (c // 8) * s_e + r * 2 + r + c for r, c in
                       (synth.rvq_matrix_shape(cfg, m) for m in (synth.GATE, synth.UP, synth.DOWN)))
-        label = "2-stage RVQ d=8" if stages is None else \
+        label = "E8P lattice code, 16 bits per 8 weights" if e8p else "2-stage RVQ d=8" if stages is None else \
             "RVQ d=8, 3/2/1 stages by popularity thirds (2 bits mean)"
         out.append({"workload": f"{cfg.name} SwiGLU MoE layer (E={cfg.E}, d={cfg.d_model}, f={cfg.d_ff}, top-8, "
                                 f"{label}), T={T}" + (" (tcgen05 path)" if T * cfg.top_k >= 16 else ""),
@@ -460,6 +465,7 @@ def extra_rows(layer, device, peak):
         guarded(one)
     guarded(lambda: _rvq_rows(device, peak))
     guarded(lambda: _rvq_rows(device, peak, synth.OLMOE_RVQ_FREQ))
+    guarded(lambda: _rvq_rows(device, peak, synth.OLMOE_E8P))
 
     def linear():
         lc = synth.LINEAR_1024x4096
@@ -671,9 +677,10 @@ def main():
     torch.cuda.set_device(device)
     if args.rvq_rows:
         if rank == 0:
+            pk = hbm_peak()[0]
             print(json.dumps({"workload": "olmoe-rvq rows (profiling case)",
-                              "rows": _rvq_rows(device, hbm_peak()[0]) + _rvq_rows(device, hbm_peak()[0],
-                                                                                 synth.OLMOE_RVQ_FREQ)}))
+                              "rows": _rvq_rows(device, pk) + _rvq_rows(device, pk, synth.OLMOE_RVQ_FREQ) +
+                              _rvq_rows(device, pk, synth.OLMOE_E8P)}))
         return 0
     t_setup = time.time()
     layer = build_dict_layer(CFG, device)

@@ -26,6 +26,7 @@ STATUS_NAMES = {0: "QMOE_OK", -1: "QMOE_EINVAL", -2: "QMOE_ECAPACITY", -3: "QMOE
 DICT_ENTRIES = 65536
 DICT_WORDS = 2 * DICT_ENTRIES
 COMPACT_BYTES = 3 * DICT_ENTRIES
+QMOE_VQ_RVQ, QMOE_VQ_E8P = 0, 1      # code formats of an RVQ matrix set
 
 EXPORTED = [
     "qmoe_encode_dictionary", "qmoe_pack", "qmoe_dict_compact", "qmoe_expert_matvec", "qmoe_route",
@@ -33,7 +34,7 @@ EXPORTED = [
     "rvq_expert_matmul", "rvq_moe_layer_ws_size", "rvq_moe_layer", "rvq_pack", "qmoe_check_status",
     "qmoe_last_error", "qmoe_decode_dense", "rvq_decode_dense", "qmoe_set_phase_events",
     "qmoe_moe_layer_noalloc", "qmoe_pack_device_ws_size", "qmoe_pack_device", "rvq_pack_stages",
-    "rvq_stage_allocation",
+    "rvq_stage_allocation", "e8p_base_table", "e8p_pack", "e8p_nearest",
 ]
 
 
@@ -64,7 +65,7 @@ class CRvqSet(ctypes.Structure):
     _fields_ = [("idx", ctypes.c_void_p), ("codebooks", ctypes.c_void_p), ("scale_f16", ctypes.c_void_p),
                 ("sign_out", ctypes.c_void_p), ("sign_in", ctypes.c_void_p), ("count", ctypes.c_int),
                 ("rows", ctypes.c_int), ("cols", ctypes.c_int), ("stages", ctypes.c_void_p),
-                ("idx_base", ctypes.c_void_p), ("n_stages", ctypes.c_int)]
+                ("idx_base", ctypes.c_void_p), ("n_stages", ctypes.c_int), ("format", ctypes.c_int)]
 
 
 _vp, _i, _sz, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
@@ -91,6 +92,9 @@ _sig = {
     "qmoe_pack_device": [_vp, _vp, _i, _i, _i, _vp, _sz, _vp, _vp, _sz, _vp],
     "rvq_pack_stages": [_vp, _i, _i, _vp, _vp, _vp, _i, _vp, _vp],
     "rvq_stage_allocation": [_vp, _i, _i, _vp],
+    "e8p_base_table": [_vp],
+    "e8p_pack": [_vp, _i, _i, _vp, _vp, _vp, _vp],
+    "e8p_nearest": [_vp, _sz, _vp],
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -192,6 +196,33 @@ def rvq_stage_allocation(popularity: np.ndarray, s_bar: int = 2) -> np.ndarray:
     return out
 
 
+def e8p_base_table() -> np.ndarray:
+    """The E8P base table: uint32 [256], nibble j of entry p = 2|a_j| of absolute pattern p."""
+    out = np.zeros(256, dtype=np.uint32)
+    _check(_lib.e8p_base_table(_np_ptr(out)), "e8p_base_table")
+    return out
+
+
+def e8p_pack(w: np.ndarray, sign_out: np.ndarray, sign_in: np.ndarray):
+    """Host E8P encoder: (code words uint16 [rows, cols/8], scale fp16 bits [rows])."""
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    rows, cols = w.shape
+    so = np.ascontiguousarray(sign_out, dtype=np.int8)
+    si = np.ascontiguousarray(sign_in, dtype=np.int8)
+    codes = np.zeros((rows, cols // 8), dtype=np.uint16)
+    sc = np.zeros(rows, dtype=np.uint16)
+    _check(_lib.e8p_pack(_np_ptr(w), rows, cols, _np_ptr(so), _np_ptr(si), _np_ptr(codes), _np_ptr(sc)), "e8p_pack")
+    return codes, sc
+
+
+def e8p_nearest(u: np.ndarray) -> np.ndarray:
+    """Code words (uint16 [n]) of the E8P codewords nearest to the rows of u [n, 8]."""
+    u = np.ascontiguousarray(u, dtype=np.float64).reshape(-1, 8)
+    out = np.zeros(u.shape[0], dtype=np.uint16)
+    _check(_lib.e8p_nearest(_np_ptr(u), u.shape[0], _np_ptr(out)), "e8p_nearest")
+    return out
+
+
 def qmoe_last_error() -> str:
     return _lib.qmoe_last_error().decode()
 
@@ -244,12 +275,23 @@ class RvqMatrixSet:
     matrix) and `idx_base` (device int64 byte offsets), matrices may have 1 .. n_stages stages each."""
 
     def __init__(self, idx, codebooks, scale_f16, sign_out, sign_in, count, rows, cols, stages=None, idx_base=None,
-                 n_stages=0):
+                 n_stages=0, fmt=QMOE_VQ_RVQ):
         self.idx, self.codebooks, self.scale, self.sign_out, self.sign_in = idx, codebooks, scale_f16, sign_out, sign_in
         self.count, self.rows, self.cols = count, rows, cols
-        self.stages, self.idx_base, self.n_stages = stages, idx_base, n_stages
+        self.stages, self.idx_base, self.n_stages, self.fmt = stages, idx_base, n_stages, fmt
         self.c = CRvqSet(_dptr(idx), _dptr(codebooks), _dptr(scale_f16), _dptr(sign_out), _dptr(sign_in), count,
-                         rows, cols, _dptr(stages), _dptr(idx_base), n_stages)
+                         rows, cols, _dptr(stages), _dptr(idx_base), n_stages, fmt)
+
+    @classmethod
+    def e8p_from_host(cls, codes, scale_f16, sign_out, sign_in, count, rows, cols, device="cuda"):
+        """E8P set: codes uint16 [count, rows, cols/8]; the base table comes from e8p_base_table."""
+        import torch
+
+        def up(a, dt, view):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=dt).view(view).copy()).to(device)
+        return cls(up(codes, np.uint16, np.int16), up(e8p_base_table(), np.uint32, np.int32),
+                   up(scale_f16, np.uint16, np.int16), up(sign_out, np.int8, np.int8), up(sign_in, np.int8, np.int8),
+                   count, rows, cols, fmt=QMOE_VQ_E8P)
 
     @classmethod
     def from_host(cls, idx, codebooks_f16, scale_f16, sign_out, sign_in, count, rows, cols, device="cuda"):

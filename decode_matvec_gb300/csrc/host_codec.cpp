@@ -7,6 +7,7 @@
 // round exactly as written so that independent exact encoders agree bit for bit.
 
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -349,6 +350,27 @@ int nearest8(const double* u, const double* cb) {
 
 bool pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 
+// W' = H_rows D_out W D_in H_cols (columns first, then rows); false on a sign outside +-1.
+bool rotate(const double* w, int rows, int cols, const int8_t* sign_out, const int8_t* sign_in,
+            std::vector<double>& a) {
+    a.assign((size_t)rows * cols, 0.0);
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            if (std::abs(sign_out[r]) != 1 || std::abs(sign_in[c]) != 1) return false;
+            a[(size_t)r * cols + c] = w[(size_t)r * cols + c] * (double)sign_out[r] * (double)sign_in[c];
+        }
+    for (int c = 0; c < cols; ++c) fwht_strided(a.data() + c, rows, (size_t)cols);
+    for (int r = 0; r < rows; ++r) fwht_strided(a.data() + (size_t)r * cols, cols, 1);
+    return true;
+}
+
+// sqrt(sum_c row[c]^2 / cols), the sum taken left to right.
+double row_rms(const double* row, int cols) {
+    double sum = 0.0;
+    for (int c = 0; c < cols; ++c) sum = sum + row[c] * row[c];
+    return std::sqrt(sum / (double)cols);
+}
+
 }  // namespace
 
 extern "C" int rvq_pack_stages(const double* w, int rows, int cols, const int8_t* sign_out,
@@ -361,22 +383,13 @@ extern "C" int rvq_pack_stages(const double* w, int rows, int cols, const int8_t
         return fail(QMOE_EINVAL, "rvq_pack: rows and cols must be powers of two in [8, 8192]");
     if (n_stages < 1 || n_stages > QMOE_RVQ_MAX_STAGES)
         return fail(QMOE_EINVAL, "rvq_pack: stage count outside 1 .. QMOE_RVQ_MAX_STAGES");
-    std::vector<double> a((size_t)rows * cols);
-    for (int r = 0; r < rows; ++r)
-        for (int c = 0; c < cols; ++c) {
-            if (std::abs(sign_out[r]) != 1 || std::abs(sign_in[c]) != 1)
-                return fail(QMOE_EINVAL, "rvq_pack: signs must be +1 or -1");
-            a[(size_t)r * cols + c] = w[(size_t)r * cols + c] * (double)sign_out[r] * (double)sign_in[c];
-        }
-    for (int c = 0; c < cols; ++c) fwht_strided(a.data() + c, rows, (size_t)cols);
-    for (int r = 0; r < rows; ++r) fwht_strided(a.data() + (size_t)r * cols, cols, 1);
+    std::vector<double> a;
+    if (!rotate(w, rows, cols, sign_out, sign_in, a)) return fail(QMOE_EINVAL, "rvq_pack: signs must be +1 or -1");
     std::vector<double> cb((size_t)n_stages * QMOE_RVQ_CODES * 8);
     for (size_t i = 0; i < cb.size(); ++i) cb[i] = half_to_double(codebooks[i]);
     for (int r = 0; r < rows; ++r) {
         const double* row = a.data() + (size_t)r * cols;
-        double sum = 0.0;
-        for (int c = 0; c < cols; ++c) sum = sum + row[c] * row[c];
-        uint16_t sh = double_to_half(std::sqrt(sum / (double)cols));
+        uint16_t sh = double_to_half(row_rms(row, cols));
         double s = half_to_double(sh);
         if (s == 0.0) return fail(QMOE_EINVAL, "rvq_pack: a row's scale rounds to zero");
         scale_f16[r] = sh;
@@ -413,6 +426,228 @@ extern "C" int rvq_stage_allocation(const double* popularity, int E, int s_bar, 
     for (int q = 0; q < E; ++q) {
         const int e = order[q];
         stages[e] = (uint8_t)(q < third ? s_bar + 1 : q >= E - third ? s_bar - 1 : s_bar);
+    }
+    return QMOE_OK;
+}
+
+// ---------------------------------------------------------------- E8P lattice code
+// "M8.5 - Extreme Weight Compression and Representations", 0x06E: a 16-bit
+// code word names a point of E8 + 1/4 = (D8^ + 1/4) u (D8^ - 1/4), where D8^
+// (= D8 + 1/2) holds the half-integer vectors with an even coordinate sum:
+// bits 0-7 pick one of 256 absolute patterns, bits 8-14 the signs of
+// coordinates 0-6, bit 15 the shift; coordinate 7's sign makes the sum even.
+namespace {
+
+constexpr double kE8pAbs[3] = {0.5, 1.5, 2.5};
+
+struct E8pTable {
+    uint32_t words[QMOE_E8P_PATTERNS];          // nibble j = 2|a_j|
+    uint8_t q[QMOE_E8P_PATTERNS][8];            // |a_j| = kE8pAbs[q]
+    uint8_t parity[QMOE_E8P_PATTERNS];          // (sum_j |a_j|) mod 2
+    int16_t index_of[6561];                     // sum_j q_j 3^j -> pattern, or -1
+};
+
+const E8pTable& e8p_table() {
+    static const E8pTable t = [] {
+        E8pTable t{};
+        // every 8-tuple over {1, 3, 5} (= 2|a|) by squared norm, then lexicographically
+        std::vector<std::array<uint8_t, 8>> all;
+        for (int n = 0; n < 6561; ++n) {
+            std::array<uint8_t, 8> d{};
+            for (int j = 0, m = n; j < 8; ++j, m /= 3) d[7 - j] = (uint8_t)(1 + 2 * (m % 3));
+            all.push_back(d);
+        }
+        auto norm = [](const std::array<uint8_t, 8>& d) {
+            int s = 0;
+            for (int v : d) s += v * v;
+            return s;
+        };
+        std::sort(all.begin(), all.end(), [&](const std::array<uint8_t, 8>& x, const std::array<uint8_t, 8>& y) {
+            const int nx = norm(x), ny = norm(y);
+            return nx != ny ? nx < ny : x < y;
+        });
+        std::fill(std::begin(t.index_of), std::end(t.index_of), (int16_t)-1);
+        for (int p = 0; p < QMOE_E8P_PATTERNS; ++p) {
+            uint32_t w = 0;
+            int sum2 = 0, key = 0, pw = 1;
+            for (int j = 0; j < 8; ++j) {
+                const int v = all[p][j];
+                w |= (uint32_t)v << (4 * j);
+                t.q[p][j] = (uint8_t)(v >> 1);
+                sum2 += v;
+                key += (v >> 1) * pw;
+                pw *= 3;
+            }
+            t.words[p] = w;
+            t.parity[p] = (uint8_t)((sum2 / 2) & 1);   // sum2 = 2 sum|a|, a sum of 8 odd numbers
+            t.index_of[key] = (int16_t)p;
+        }
+        return t;
+    }();
+    return t;
+}
+
+struct E8pBest {
+    double d = INFINITY;
+    uint32_t code = 0x10000u;
+};
+
+// Codeword of code word `code` (pattern p, coordinate signs neg[], shift c) and its squared
+// distance to u, summed over j = 0..7 in order; kept when (d, code) is the smallest so far.
+void e8p_consider(const double* u, int p, const bool* neg, int b, E8pBest& best) {
+    const E8pTable& t = e8p_table();
+    const double c = b ? 0.25 : -0.25;
+    double d = 0.0;
+    uint32_t code = (uint32_t)p | ((uint32_t)b << 15);
+    for (int j = 0; j < 8; ++j) {
+        const double a = kE8pAbs[t.q[p][j]];
+        const double v = (neg[j] ? -a : a) + c;
+        const double diff = u[j] - v;
+        d = d + diff * diff;
+        if (j < 7 && neg[j]) code |= 1u << (8 + j);
+    }
+    if (d < best.d || (d == best.d && code < best.code)) {
+        best.d = d;
+        best.code = code;
+    }
+}
+
+// Nearest point of D8^ + c (Conway and Sloane's decoder for D8, on the half-integer grid);
+// false when the rounding or the parity repair is ambiguous or the pattern is not in the table.
+bool e8p_lattice(const double* u, int b, int& p_out, bool (&neg)[8]) {
+    const E8pTable& t = e8p_table();
+    const double c = b ? 0.25 : -0.25;
+    double h[8], err[8], sum = 0.0;
+    for (int j = 0; j < 8; ++j) {
+        const double w = u[j] - c;
+        const double fl = std::floor(w);
+        if (w == fl) return false;                      // equidistant from two half-integers
+        h[j] = fl + 0.5;
+        err[j] = w - h[j];
+        sum += h[j];
+    }
+    if (std::fmod(std::fabs(sum), 2.0) != 0.0) {        // odd sum: move the worst coordinate
+        int k = 0;
+        for (int j = 1; j < 8; ++j)
+            if (std::fabs(err[j]) > std::fabs(err[k])) k = j;
+        for (int j = 0; j < 8; ++j)
+            if (j != k && std::fabs(err[j]) == std::fabs(err[k])) return false;
+        h[k] += err[k] > 0 ? 1.0 : -1.0;
+    }
+    int key = 0, pw = 1;
+    for (int j = 0; j < 8; ++j) {
+        const double a = std::fabs(h[j]);
+        const int q = a == 0.5 ? 0 : a == 1.5 ? 1 : a == 2.5 ? 2 : -1;
+        if (q < 0) return false;
+        key += q * pw;
+        pw *= 3;
+        neg[j] = h[j] < 0;
+    }
+    p_out = t.index_of[key];
+    return p_out >= 0;
+}
+
+// Nearest codeword of shift b over all 256 patterns: per pattern the optimal signs (each
+// coordinate takes the sign of u_j - c; a wrong parity flips the coordinate where that
+// costs least, 4 |u_j - c| |a_j|), then the exact distances of the near-best candidates.
+void e8p_search(const double* u, int b, E8pBest& best) {
+    const E8pTable& t = e8p_table();
+    const double c = b ? 0.25 : -0.25;
+    double m[8], e[8][3], f[8][3];
+    bool neg0[8];
+    int n_neg = 0;
+    for (int j = 0; j < 8; ++j) {
+        const double w = u[j] - c;
+        neg0[j] = w < 0;
+        n_neg += neg0[j];
+        m[j] = std::fabs(w);
+        for (int q = 0; q < 3; ++q) {
+            const double dq = m[j] - kE8pAbs[q];
+            e[j][q] = dq * dq;
+            f[j][q] = m[j] * kE8pAbs[q];
+        }
+    }
+    double D[QMOE_E8P_PATTERNS], dmin = INFINITY;
+    for (int p = 0; p < QMOE_E8P_PATTERNS; ++p) {
+        double s = 0.0;
+        for (int j = 0; j < 8; ++j) s += e[j][t.q[p][j]];
+        if ((n_neg + t.parity[p]) & 1) {
+            double fm = f[0][t.q[p][0]];
+            for (int j = 1; j < 8; ++j) fm = std::min(fm, f[j][t.q[p][j]]);
+            s += 4.0 * fm;
+        }
+        D[p] = s;
+        dmin = std::min(dmin, s);
+    }
+    const double cut = dmin + 1e-9 * (1.0 + dmin);
+    for (int p = 0; p < QMOE_E8P_PATTERNS; ++p) {
+        if (D[p] > cut) continue;
+        if (!((n_neg + t.parity[p]) & 1)) {
+            e8p_consider(u, p, neg0, b, best);
+            continue;
+        }
+        double fm = f[0][t.q[p][0]];
+        for (int j = 1; j < 8; ++j) fm = std::min(fm, f[j][t.q[p][j]]);
+        for (int k = 0; k < 8; ++k) {
+            if (f[k][t.q[p][k]] != fm) continue;
+            bool neg[8];
+            for (int j = 0; j < 8; ++j) neg[j] = neg0[j] != (j == k);
+            e8p_consider(u, p, neg, b, best);
+        }
+    }
+}
+
+uint16_t e8p_encode8(const double* u) {
+    E8pBest best;
+    for (int b = 0; b < 2; ++b) {
+        int p;
+        bool neg[8];
+        if (e8p_lattice(u, b, p, neg)) e8p_consider(u, p, neg, b, best);
+        else e8p_search(u, b, best);
+    }
+    return (uint16_t)best.code;
+}
+
+}  // namespace
+
+extern "C" int e8p_base_table(uint32_t* table) {
+    qmoe::clear_error();
+    if (!table) return fail(QMOE_EINVAL, "e8p_base_table: NULL argument");
+    std::memcpy(table, e8p_table().words, sizeof(e8p_table().words));
+    return QMOE_OK;
+}
+
+extern "C" int e8p_pack(const double* w, int rows, int cols, const int8_t* sign_out, const int8_t* sign_in,
+                        uint16_t* codes, uint16_t* scale_f16) {
+    qmoe::clear_error();
+    if (!w || !sign_out || !sign_in || !codes || !scale_f16) return fail(QMOE_EINVAL, "e8p_pack: NULL argument");
+    if (!pow2(rows) || !pow2(cols) || cols % 8 || rows > 8192 || cols > 8192)
+        return fail(QMOE_EINVAL, "e8p_pack: rows and cols must be powers of two in [8, 8192]");
+    std::vector<double> a;
+    if (!rotate(w, rows, cols, sign_out, sign_in, a)) return fail(QMOE_EINVAL, "e8p_pack: signs must be +1 or -1");
+    const double kappa = std::sqrt(2450.0 / 2048.0);
+    for (int r = 0; r < rows; ++r) {
+        const double* row = a.data() + (size_t)r * cols;
+        const uint16_t sh = double_to_half(row_rms(row, cols) / kappa);
+        const double s = half_to_double(sh);
+        if (s == 0.0) return fail(QMOE_EINVAL, "e8p_pack: a row's scale rounds to zero");
+        scale_f16[r] = sh;
+        for (int v = 0; v < cols / 8; ++v) {
+            double u[8];
+            for (int k = 0; k < 8; ++k) u[k] = row[v * 8 + k] / s;
+            codes[(size_t)r * (cols / 8) + v] = e8p_encode8(u);
+        }
+    }
+    return QMOE_OK;
+}
+
+extern "C" int e8p_nearest(const double* u, size_t n, uint16_t* codes) {
+    qmoe::clear_error();
+    if ((!u || !codes) && n) return fail(QMOE_EINVAL, "e8p_nearest: NULL argument");
+    for (size_t i = 0; i < n; ++i) {
+        for (int j = 0; j < 8; ++j)
+            if (!std::isfinite(u[i * 8 + j])) return fail(QMOE_EINVAL, "e8p_nearest: non-finite input");
+        codes[i] = e8p_encode8(u + i * 8);
     }
     return QMOE_OK;
 }

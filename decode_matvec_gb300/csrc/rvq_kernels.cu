@@ -36,12 +36,14 @@ struct RvqDev {
     int count, rows, cols;
     const uint8_t* stages;     // per matrix stage count, or NULL (2)
     const uint64_t* idx_base;  // per matrix byte offset of its codes, or NULL
-    int n_st;                  // codebooks in the set
+    int n_st;                  // codebooks in the set (0 for E8P)
+    int e8p;                   // E8P lattice code words instead of codebook indices
 };
 
 RvqDev to_dev(const rvq_matrix_set* s) {
+    const bool e8p = s->format == QMOE_VQ_E8P;
     return RvqDev{s->idx, s->codebooks, s->scale_f16, s->sign_out, s->sign_in, s->count, s->rows, s->cols,
-                  s->stages, s->idx_base, s->n_stages ? s->n_stages : 2};
+                  s->stages, s->idx_base, e8p ? 0 : s->n_stages ? s->n_stages : 2, e8p ? 1 : 0};
 }
 
 // Stage count of matrix e, or 0 for a count outside 1 .. n_st: that records
@@ -67,7 +69,70 @@ bool pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
 bool valid_set(const rvq_matrix_set* s) {
     return s && s->idx && s->codebooks && s->scale_f16 && s->sign_out && s->sign_in && s->count >= 1 &&
            pow2(s->rows) && pow2(s->cols) && s->cols >= 8 && s->rows <= 8192 && s->cols <= 8192 &&
-           s->n_stages >= 0 && s->n_stages <= QMOE_RVQ_MAX_STAGES && (s->stages || s->n_stages != 1);
+           s->n_stages >= 0 && s->n_stages <= QMOE_RVQ_MAX_STAGES && (s->stages || s->n_stages != 1) &&
+           (s->format == QMOE_VQ_RVQ || (s->format == QMOE_VQ_E8P && !s->stages && s->n_stages == 0));
+}
+
+// ---------------------------------------------------------------- E8P decode
+// ("M8.5 - Extreme Weight Compression and Representations", 0x06E.)  The base
+// table arrives as 256 words of 8 nibbles 2|a_j|; shared memory holds it as
+// 8 bytes per pattern (byte j = 2|a_j|), replicated so that the lanes of a
+// warp read different banks.  A code word's 8 coordinates come out as four
+// exact fp16 pairs: a byte permute puts 2|a_j| under the fp16 exponent of
+// 1024 (the value 1024 + 2|a_j|), one fp16x2 multiply-add makes |a_j|, the
+// sign bits are spread onto the two halves' sign bits with one multiply, and
+// one fp16x2 add applies the +-1/4 shift.  Every coordinate is a multiple of
+// 1/4 below 3, so every step is exact.
+constexpr int kE8pRepGemm = 16;   // table replicas in rvq_gemm_kernel (8-byte entries: 16 banks pairs)
+constexpr int kE8pRepTc = 4;      // table replicas in rvq_tc_kernel
+
+__device__ __forceinline__ uint2 e8p_bytes(uint32_t w) {
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        lo |= ((w >> (4 * j)) & 15u) << (8 * j);
+        hi |= ((w >> (16 + 4 * j)) & 15u) << (8 * j);
+    }
+    return make_uint2(lo, hi);
+}
+
+// table[p * rep + r] = pattern p's bytes, r = 0 .. rep-1.  Every thread of the block calls it.
+__device__ __forceinline__ void e8p_stage_table(const uint32_t* __restrict__ g, uint2* t, int rep) {
+    for (int i = threadIdx.x; i < 256 * rep; i += blockDim.x) t[i] = e8p_bytes(__ldg(g + i / rep));
+}
+
+__device__ __forceinline__ void e8p_half8(uint2 pb, uint32_t code, uint32_t (&h)[4]) {
+    // sum_j 2|a_j| = 2 sum_j |a_j|; coordinate 7 is negative when the explicit negatives
+    // leave sum_j s_j |a_j| odd
+    const uint32_t two_sum = __dp4a(pb.x, 0x01010101u, __dp4a(pb.y, 0x01010101u, 0u));
+    const uint32_t sg = (code >> 8) & 127u;
+    const uint32_t neg = sg | ((((two_sum >> 1) + (uint32_t)__popc(sg)) & 1u) << 7);
+    const uint32_t c2 = (code & 0x8000u) ? 0x34003400u : 0xB400B400u;   // (+1/4, +1/4) or (-1/4, -1/4)
+    const __half2 half = __floats2half2_rn(0.5f, 0.5f), m512 = __floats2half2_rn(-512.0f, -512.0f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t src = q < 2 ? pb.x : pb.y;
+        // fp16 lanes 0x64nn = 1024 + n: bytes (n_2q, 0x64, n_2q+1, 0x64), 0x64 from byte 1 / 3 of the constant
+        const uint32_t sel = (uint32_t)((2 * q) & 3) | (5u << 4) | ((uint32_t)((2 * q + 1) & 3) << 8) | (7u << 12);
+        const uint32_t m = __byte_perm(src, 0x64006400u, sel);
+        const __half2 a = __hfma2(*reinterpret_cast<const __half2*>(&m), half, m512);
+        // (y * 0x40008000) & 0x80008000 moves bit 0 of y to bit 15 and bit 1 to bit 31
+        const uint32_t sm = ((neg >> (2 * q)) * 0x40008000u) & 0x80008000u;
+        const uint32_t sa = *reinterpret_cast<const uint32_t*>(&a) ^ sm;
+        const __half2 v = __hadd2(*reinterpret_cast<const __half2*>(&sa), *reinterpret_cast<const __half2*>(&c2));
+        h[q] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+}
+
+__device__ __forceinline__ void e8p_float8(uint2 pb, uint32_t code, float (&w)[8]) {
+    uint32_t h[4];
+    e8p_half8(pb, code, h);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[q]));
+        w[2 * q] = f.x;
+        w[2 * q + 1] = f.y;
+    }
 }
 
 // Normalised Walsh-Hadamard transform of n floats in shared memory, in place.
@@ -229,7 +294,8 @@ __device__ __forceinline__ void decode_vec(const uint4* cb, const uint32_t (&cod
     }
 }
 
-template <int NT, int S>
+// E8: the codes are E8P code words (S = 2 bytes each) and scb holds the staged E8P table.
+template <int NT, int S, bool E8 = false>
 __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const float* xs, const Job& job, int r0,
                               int warp, int nwarps, int lane) {
     const RvqDev& m = a.m;
@@ -242,17 +308,22 @@ __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const floa
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
         for (int v = lane; v < nv; v += 32) {
-            uint32_t code[S];
-            if constexpr (S == 2) {
-                const uint32_t pr = __ldg((const uint16_t*)ip + v);
-                code[0] = pr & 255u;
-                code[1] = pr >> 8;
-            } else {
-#pragma unroll
-                for (int st = 0; st < S; ++st) code[st] = __ldg(ip + (size_t)v * S + st);
-            }
             float w[8];
-            decode_vec<S>(scb, code, w);
+            if constexpr (E8) {
+                const uint32_t cw = __ldg((const uint16_t*)ip + v);
+                e8p_float8(((const uint2*)scb)[(cw & 255u) * kE8pRepGemm + (lane & (kE8pRepGemm - 1))], cw, w);
+            } else {
+                uint32_t code[S];
+                if constexpr (S == 2) {
+                    const uint32_t pr = __ldg((const uint16_t*)ip + v);
+                    code[0] = pr & 255u;
+                    code[1] = pr >> 8;
+                } else {
+#pragma unroll
+                    for (int st = 0; st < S; ++st) code[st] = __ldg(ip + (size_t)v * S + st);
+                }
+                decode_vec<S>(scb, code, w);
+            }
             if constexpr (NT == 1) {
                 const float4 x0 = ((const float4*)xs)[2 * v], x1 = ((const float4*)xs)[2 * v + 1];
                 acc[0] = fmaf(w[0], x0.x, acc[0]);
@@ -308,12 +379,15 @@ __device__ void rvq_stage(const RvqGemmArgs& a, const Job& job, float* xs) {
     }
 }
 
-__global__ void __launch_bounds__(kRvqThreads) rvq_gemm_kernel(const RvqGemmArgs a) {
+// two blocks per SM (the launch grid): up to 128 registers a thread
+__global__ void __launch_bounds__(kRvqThreads, 2) rvq_gemm_kernel(const RvqGemmArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    uint4* scb = (uint4*)smem;                  // [n_st][256] x 8 fp16
-    float* xs = (float*)(smem + (size_t)a.m.n_st * 256 * 16);
+    uint4* scb = (uint4*)smem;                  // [n_st][256] x 8 fp16, or the replicated E8P table
+    float* xs = (float*)(smem + (a.m.e8p ? (size_t)256 * kE8pRepGemm * 8 : (size_t)a.m.n_st * 256 * 16));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    for (int i = tid; i < a.m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)a.m.cb + i);
+    if (a.m.e8p) e8p_stage_table((const uint32_t*)a.m.cb, (uint2*)smem, kE8pRepGemm);
+    else
+        for (int i = tid; i < a.m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)a.m.cb + i);
     __syncthreads();
     const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
     const int n_tiles = n_jobs * a.row_tiles;
@@ -342,7 +416,11 @@ __global__ void __launch_bounds__(kRvqThreads) rvq_gemm_kernel(const RvqGemmArgs
         }
         __syncthreads();
         const int S = stages_of(a.m, job.matrix);
-        if (S == 0) {
+        if (a.m.e8p) {
+            if (nt == 1) rvq_tile_rows<1, 2, true>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else if (nt == 4) rvq_tile_rows<4, 2, true>(a, scb, xs, job, r0, warp, nwarps, lane);
+            else rvq_tile_rows<8, 2, true>(a, scb, xs, job, r0, warp, nwarps, lane);
+        } else if (S == 0) {
             // nothing
         } else if (S == 2) {
             if (nt == 1) rvq_tile_rows<1, 2>(a, scb, xs, job, r0, warp, nwarps, lane);
@@ -448,6 +526,20 @@ __device__ __forceinline__ void stage_run(const uint4* scb, const uint2 (&cw)[QM
     }
 }
 
+// A thread's kTcVpt consecutive E8P code words (16 bytes in cw[0], cw[1]) decoded to exact
+// fp16 rows of its weight-tile row.
+__device__ __forceinline__ void e8p_run(const uint2* tab, const uint2 (&cw)[QMOE_RVQ_MAX_STAGES], int lane,
+                                        unsigned char* dst) {
+#pragma unroll
+    for (int q = 0; q < kTcVpt; ++q) {
+        const uint32_t word = q < 4 ? (q < 2 ? cw[0].x : cw[0].y) : (q < 6 ? cw[1].x : cw[1].y);
+        const uint32_t code = (word >> (16 * (q & 1))) & 0xFFFFu;
+        uint32_t h[4];
+        e8p_half8(tab[(code & 255u) * kE8pRepTc + (lane & (kE8pRepTc - 1))], code, h);
+        *(uint4*)(dst + q * kTcLBO) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
 // fp16 high part of 8 values, and the fp16 of what the high part leaves.
 __device__ __forceinline__ void store_hi_lo8(uint8_t* hi, uint8_t* lo, const float (&v)[8]) {
     __half2 h[4], l[4];
@@ -472,7 +564,9 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const RvqDev& m = a.m;
 
-    for (int i = tid; i < m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)m.cb + i);
+    if (m.e8p) e8p_stage_table((const uint32_t*)m.cb, (uint2*)scb, kE8pRepTc);
+    else
+        for (int i = tid; i < m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)m.cb + i);
     if (tid == 0) {
         for (int b = 0; b < 2; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + b)) : "memory");
@@ -553,7 +647,8 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
             }
             uint8_t* Bh = bbuf + (kc & 1) * 2 * kTcBBytes;           // N = 64 rows: high parts, then low
             uint8_t* Bl = Bh + 4 * kTcSBO;
-            for (int st = 0; st < S; ++st) {
+            const int n_steps = m.e8p ? 1 : S;                // E8P: one exact fp16 tile per chunk
+            for (int st = 0; st < n_steps; ++st) {
                 const int b = gs & 1u;
                 if (gs >= 2 && done + 1 < gs) {
                     // step gs - 2 (and so every earlier step: chunk kc - 2 included) has finished
@@ -566,6 +661,8 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
                 if (arow >= m.rows) {
 #pragma unroll
                     for (int q = 0; q < kTcVpt; ++q) *(uint4*)(arow_base + q * kTcLBO) = make_uint4(0, 0, 0, 0);
+                } else if (m.e8p) {
+                    e8p_run((const uint2*)scb, cw, lane, arow_base);
                 } else {
                     stage_run(scb, cw, S, st, arow_base);
                 }
@@ -673,7 +770,10 @@ __global__ void rvq_decode_kernel(RvqDev m, float* __restrict__ out) {
     const uint8_t* ip = codes_of(m, 0) + v * S;
     const uint4* cb = (const uint4*)m.cb;
     float w[8];
-    if (S == 0) {
+    if (m.e8p) {
+        const uint32_t code = ((const uint16_t*)codes_of(m, 0))[v];
+        e8p_float8(e8p_bytes(__ldg((const uint32_t*)m.cb + (code & 255u))), code, w);
+    } else if (S == 0) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) w[j] = 0.0f;
     } else if (S == 1) {
@@ -698,7 +798,8 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 // are about two tiles per SM.
 int launch_rvq_gemm(RvqGemmArgs a, cudaStream_t st, long long jobs_hint) {
     const int sms = qmoe::sm_count();
-    const size_t smem = (size_t)a.m.n_st * 256 * 16 + (size_t)a.m.cols * a.nt_max * 4;
+    const size_t tab = a.m.e8p ? (size_t)256 * kE8pRepGemm * 8 : (size_t)a.m.n_st * 256 * 16;
+    const size_t smem = tab + (size_t)a.m.cols * a.nt_max * 4;
     int rc = qmoe::cuda_check(
         cudaFuncSetAttribute(rvq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem), "rvq attr");
     if (rc) return rc;

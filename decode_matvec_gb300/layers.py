@@ -13,7 +13,7 @@ import os
 
 import numpy as np
 
-from . import (Dictionary, MatrixSet, RvqMatrixSet, qmoe_encode_dictionary, qmoe_pack_into, rvq_pack)
+from . import (Dictionary, MatrixSet, RvqMatrixSet, e8p_pack, qmoe_encode_dictionary, qmoe_pack_into, rvq_pack)
 
 
 def _threads(n: int | None) -> int:
@@ -121,3 +121,24 @@ def pack_rvq_set(count: int, rows: int, cols: int, codebooks_f16: np.ndarray, we
     idx = np.stack(per) if stages is None else per
     return RvqMatrixSet.from_host(idx, cb if stages is not None else cb[:2], scales.reshape(-1), so.reshape(-1),
                                   si.reshape(-1), count, rows, cols, device=device)
+
+
+def pack_e8p_set(count: int, rows: int, cols: int, weight_fn, sign_fn, threads: int | None = None,
+                 device="cuda") -> RvqMatrixSet:
+    """Encode `count` matrices with the E8P lattice code: weight_fn(e) -> float64 [rows, cols],
+    sign_fn(e) -> (sign_out, sign_in)."""
+    codes = np.zeros((count, rows, cols // 8), dtype=np.uint16)
+    scales = np.zeros((count, rows), dtype=np.uint16)
+    so = np.zeros((count, rows), dtype=np.int8)
+    si = np.zeros((count, cols), dtype=np.int8)
+
+    def work(e):
+        w = weight_fn(e)
+        s_out, s_in = sign_fn(e)
+        codes[e], scales[e] = e8p_pack(w, s_out, s_in)
+        so[e], si[e] = s_out, s_in
+
+    with cf.ThreadPoolExecutor(max_workers=_threads(threads)) as ex:
+        list(ex.map(work, range(count)))
+    return RvqMatrixSet.e8p_from_host(codes, scales.reshape(-1), so.reshape(-1), si.reshape(-1), count, rows, cols,
+                                      device=device)

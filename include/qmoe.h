@@ -65,6 +65,11 @@ typedef enum {
 #define QMOE_RVQ_CODES 256
 /* most residual stages an RVQ code may have */
 #define QMOE_RVQ_MAX_STAGES 3
+/* code formats of an rvq_matrix_set */
+#define QMOE_VQ_RVQ 0 /* residual k-means codebooks: one 8-bit index per stage */
+#define QMOE_VQ_E8P 1 /* E8P lattice code: one 16-bit word per 8-vector */
+/* entries of the E8P base table (absolute patterns) */
+#define QMOE_E8P_PATTERNS 256
 
 /* ======================================================================
  * Host-side codec (dictionary format)
@@ -305,7 +310,19 @@ int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_set* wi,
  * fp32(s_r) * (((fp32(C1[i1][j]) + fp32(C2[i2][j])) + fp32(C3[i3][j])) ...),
  * the adds left to right over the matrix's stages; layer output
  * y = D_out H_rows (W' (H_cols D_in x)) with H the normalised Walsh-Hadamard
- * matrix.  Zero-initialising the last three fields gives the two-stage set.
+ * matrix.  Zero-initialising the last four fields gives the two-stage set.
+ *
+ * format QMOE_VQ_E8P ("M8.5 - Extreme Weight Compression and
+ * Representations", 0x06E): the same transforms and per-row scales, and
+ *  idx       device uint16 code words, little-endian, [rows][cols/8] per
+ *            matrix (2 bytes per vector: the offsets above with S_e = 2);
+ *  codebooks device uint32 [256]: the base table of e8p_base_table;
+ *  stages    NULL and n_stages 0.
+ * Code word c decodes to the 8-vector v: pattern p = c & 255, nibble j of
+ * table[p] is 2|a_j| (1, 3 or 5); coordinate j < 7 is negative when bit 8+j
+ * is set, coordinate 7 when that makes sum_j s_j |a_j| odd otherwise (so the
+ * sum is even: a point of D8 + 1/2); v_j = s_j |a_j| + (bit 15 ? 1/4 : -1/4).
+ * Decoded rotated weight: W'[r][8v+j] = fp32(s_r) * v_j (exact in fp32).
  */
 typedef struct {
     const uint8_t* idx;
@@ -317,6 +334,7 @@ typedef struct {
     const uint8_t* stages;
     const uint64_t* idx_base;
     int n_stages;
+    int format; /* QMOE_VQ_RVQ (0) or QMOE_VQ_E8P */
 } rvq_matrix_set;
 
 /* Workspace bytes for rvq_expert_matmul. */
@@ -393,6 +411,37 @@ int rvq_pack_stages(const double* w, int rows, int cols, const int8_t* sign_out,
  */
 int rvq_stage_allocation(const double* popularity, int E, int s_bar, uint8_t* stages);
 
+/*
+ * The E8P base table ("M8.5 - Extreme Weight Compression and
+ * Representations", 0x06E: 8 bits select one of 256 stored absolute
+ * patterns, 1 KiB): the 256 patterns a in {1/2, 3/2, 5/2, ...}^8 of smallest
+ * squared norm, equal norms in lexicographic order of (2a_0, .., 2a_7);
+ * entry p holds 2a_j in bits 4j .. 4j+3.
+ *  table host out uint32 [256].  Errors: EINVAL (NULL).
+ */
+int e8p_base_table(uint32_t* table);
+
+/*
+ * Host-side E8P encoder for one matrix: the rotated weight W' as in rvq_pack,
+ * per-row scale s_r = fp16(sqrt(sum_c W'^2 / cols) / kappa) (sum left to
+ * right; kappa^2 = 2450/2048, the mean power per coordinate of the 65 536
+ * codewords), u = W'/s_r cut into 8-vectors, and for each the code word of
+ * the nearest codeword (squared distance summed over j = 0..7 in float64;
+ * ties to the smaller code word).
+ *  w host float64 [rows][cols];  sign_out/sign_in host int8 +-1;
+ *  codes host out uint16 [rows][cols/8];  scale_f16 host out [rows].
+ * Errors: EINVAL (shape: powers of two, cols % 8; null; a zero row).
+ */
+int e8p_pack(const double* w, int rows, int cols, const int8_t* sign_out,
+             const int8_t* sign_in, uint16_t* codes, uint16_t* scale_f16);
+
+/*
+ * The encoder's search alone: for each of n 8-vectors u (host float64
+ * [n][8]) the code word of the nearest E8P codeword, as in e8p_pack.
+ *  codes host out uint16 [n].  Errors: EINVAL (NULL with n > 0, non-finite u).
+ */
+int e8p_nearest(const double* u, size_t n, uint16_t* codes);
+
 /* ======================================================================
  * Status and test exports
  * ====================================================================== */
@@ -427,8 +476,8 @@ const char* qmoe_last_error(void);
 int qmoe_decode_dense(const qmoe_dict* dict, const qmoe_matrix_set* mat,
                       float* w_out, void* stream);
 
-/* Test export: decoded rotated RVQ weight W', device fp32 [rows][cols]
- * (count == 1). */
+/* Test export: decoded rotated RVQ or E8P weight W', device fp32
+ * [rows][cols] (count == 1). */
 int rvq_decode_dense(const rvq_matrix_set* mat, float* w_out, void* stream);
 
 #ifdef __cplusplus

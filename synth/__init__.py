@@ -40,6 +40,7 @@ TAG_RVQ_W = 6
 TAG_RVQ_SIGN = 7
 TAG_KMEANS = 8
 TAG_ZIPF_RANK = 9
+TAG_E8P = 10
 
 
 def splitmix64_scalar(key: int, idx: int) -> int:
@@ -183,6 +184,16 @@ def rvq_weight(seed: int, expert: int, matrix: int, rows: int, cols: int, std: f
     return rng.normal(0.0, std, size=(rows, cols))
 
 
+def e8p_random_matrix(seed: int, expert: int, matrix: int, rows: int, cols: int, std: float = 0.02):
+    """Uniform 16-bit code words uint16 [rows, cols/8] (every word is an E8P code word) and fp16
+    row-scale bits [rows] drawn from U(0.5, 1.5) * std / 1.094 (the scale a N(0, std^2) weight
+    gets), for parity cases that need no encoder."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, TAG_E8P, expert, matrix]))
+    codes = rng.integers(0, 1 << 16, size=(rows, cols // 8)).astype(np.uint16)
+    scale = (rng.uniform(0.5, 1.5, size=rows) * std / 1.094).astype(np.float16).view(np.uint16)
+    return codes, scale
+
+
 def rvq_signs(seed: int, expert: int, matrix: int, n_out: int, n_in: int) -> tuple[np.ndarray, np.ndarray]:
     """Random sign diagonals (output side, input side) as int8 +-1."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, TAG_RVQ_SIGN, expert, matrix]))
@@ -235,6 +246,8 @@ class RvqLayer:
     # frequency-conditioned stages: router with the layer's fixed Zipf popularity, and per-expert
     # stage counts stages-1 / stages / stages+1 for the least / middle / most popular thirds
     freq_stages: bool = False
+    # "rvq": residual k-means codebooks; "e8p": the E8P lattice code (one 16-bit word per 8 weights)
+    vq: str = "rvq"
 
 
 LINEAR_1024x4096 = LinearCfg("linear-1024x4096-p0.89", 1024, 4096, 0.89, 0, (1, 8, 32))
@@ -243,6 +256,7 @@ SWITCH_LARGE_128 = DictLayer("switch-large-128", 128, 1024, 4096, 0.87, 2, 1, "z
 SWITCH_C2048 = DictLayer("switch-c2048", 2048, 2080, 6144, 0.886, 3, 1, "zipf", 1.0, (1, 64, 4096))
 OLMOE_RVQ = RvqLayer("olmoe-rvq-2bit", 64, 2048, 1024, 4, 8, 0.9, (1, 32))
 OLMOE_RVQ_FREQ = RvqLayer("olmoe-rvq-freq-2bit", 64, 2048, 1024, 4, 8, 0.9, (1, 32), freq_stages=True)
+OLMOE_E8P = RvqLayer("olmoe-e8p-2bit", 64, 2048, 1024, 4, 8, 0.9, (1, 32), vq="e8p")
 
 # matrix ids inside a dictionary-coded expert
 WI, WO = 0, 1

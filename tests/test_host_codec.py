@@ -168,3 +168,52 @@ def test_three_stage_codebook_fixture_extends_the_two_stage_one():
     cb3 = np.load(os.path.join(golden, "olmoe_rvq_codebooks3.npy"))
     assert cb2.shape == (2, 256, 8) and cb3.shape == (3, 256, 8)
     assert np.array_equal(cb3[:2].view(np.uint16), cb2.view(np.uint16))
+
+
+def test_e8p_base_table_matches_oracle():
+    from oracle import e8p as P8
+    assert np.array_equal(Q.e8p_base_table(), P8.base_table_words())
+
+
+@pytest.mark.parametrize("rows,cols,seed", [(16, 64, 0), (8, 256, 1), (32, 32, 2)])
+def test_e8p_pack_matches_oracle(rows, cols, seed):
+    from oracle import e8p as P8
+    w = synth.rvq_weight(4, seed, 2, rows, cols)
+    so, si = synth.rvq_signs(4, seed, 2, rows, cols)
+    codes, sc = Q.e8p_pack(w, so, si)
+    rcodes, rsc = P8.encode(R.rotate_weight(w, so, si))
+    assert np.array_equal(sc, rsc)
+    assert np.array_equal(codes, rcodes)
+
+
+def test_e8p_nearest_matches_brute_force_on_boundaries_and_far_points():
+    """The host search (lattice decoder first, all patterns when that is ambiguous or outside
+    the table) against the oracle's brute force: Voronoi-boundary inputs, where ties go to the
+    smaller code word, points far outside the codebook, and exact codewords."""
+    from oracle import e8p as P8
+    rng = np.random.default_rng(4)
+    special = np.array([[0.0] * 8, [1.0] * 8, [0.25] * 8, [-0.25] * 8, [0.5] * 8, [-0.75] * 8,
+                        [-0.25, 0.25, 1.0, -1.0, 2.0, 0.5, -0.5, 0.0], [3.0, -3.0, 0.0, 0.0, 1.0, 1.0, -1.0, 2.0],
+                        [0.75, 0.75, 0.75, 0.75, 0.25, 0.25, 0.25, 0.25], [9.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, -9.0]])
+    far = rng.standard_normal((200, 8)) * 3.0
+    near = rng.standard_normal((600, 8)) * np.sqrt(P8.kappa_squared())
+    grid = rng.integers(-8, 9, (200, 8)) / 4.0                      # quarter-integers: many exact ties
+    cw = P8.decode_codes(rng.integers(0, 65536, 100))
+    u = np.vstack([special, far, near, grid, cw])
+    assert np.array_equal(Q.e8p_nearest(u), P8.nearest_codes(u))
+    with pytest.raises(Q.QmoeError):
+        Q.e8p_nearest(np.full((1, 8), np.nan))
+
+
+def test_e8p_pack_codewords_round_trip():
+    """A weight whose rotated rows are scaled codewords encodes to those code words."""
+    from oracle import e8p as P8
+    rng = np.random.default_rng(5)
+    rows, cols = 8, 64
+    codes = rng.integers(0, 65536, (rows, cols // 8)).astype(np.uint16)
+    wr = P8.decode_codes(codes).reshape(rows, cols)
+    so, si = synth.rvq_signs(4, 9, 0, rows, cols)
+    w = R.unrotate_weight(wr, so, si)
+    got, sc = Q.e8p_pack(w, so, si)
+    want, wsc = P8.encode(R.rotate_weight(w, so, si))
+    assert np.array_equal(sc, wsc) and np.array_equal(got, want)
