@@ -383,6 +383,27 @@ def _dict_layer_row(layer, cfg, T, device, peak, note=""):
             "stream_bytes": sb, "stream_gbs": sb / t / 1e9, "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak}
 
 
+def _rvq_phases(call, K=20):
+    """Device time of rvq_moe_layer's phases (library phase events), averaged over K calls."""
+    import torch
+    import decode_matvec_gb300 as Q
+    st = torch.cuda.current_stream()
+    pool = []
+    for _ in range(K):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for e in ev:
+            e.record(st)        # torch creates the CUDA event on first record
+        pool.append(ev)
+    torch.cuda.synchronize()
+    for ev in pool:
+        Q.qmoe_set_phase_events(ev)
+        call()
+    Q.qmoe_set_phase_events(None)
+    torch.cuda.synchronize()
+    names = ("plan_and_in_transform", "gate_up", "swiglu_and_down_in_transform", "down", "out_transform")
+    return {n: sum(ev[i].elapsed_time(ev[i + 1]) for ev in pool) / K for i, n in enumerate(names)}
+
+
 def _rvq_rows(device, peak, cfg=None):
     """The OLMoE-shaped RVQ layer at T = 1 and 32.  With cfg.freq_stages, expert e's matrices have
     rvq_stage_allocation(popularity)[e] stages (3 / 2 / 1 by popularity thirds, mean 2 bits per
@@ -423,6 +444,8 @@ def _rvq_rows(device, peak, cfg=None):
             Q.qmoe_route(lg, cfg.top_k, ids, gates)
             Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws, y_is_f32=False)
         t = _time_calls(step)
+        phases = _rvq_phases(lambda: Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws,
+                                                     y_is_f32=False))
         touched = np.unique(ids.cpu().numpy().reshape(-1))
         sb = 1024 if e8p else 2 * 256 * 8 * cb.shape[0]
         for e in touched:
@@ -435,7 +458,7 @@ def _rvq_rows(device, peak, cfg=None):
                                 f"{label}), T={T}" + (" (tcgen05 path)" if T * cfg.top_k >= 16 else ""),
                     "tokens_per_s": T / t, "ms_per_call": t * 1e3, "touched_experts": int(len(touched)),
                     "stream_bytes": int(sb), "stream_gbs": sb / t / 1e9,
-                    "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak})
+                    "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak, "phase_ms": phases})
     return out
 
 
@@ -642,8 +665,9 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling case: keep only this many experts of the c2048-shaped layer")
     ap.add_argument("--tokens", type=int, default=None, help="profiling case: token batch size")
-    ap.add_argument("--rvq-rows", action="store_true",
-                    help="profiling case: only the OLMoE-shaped RVQ layer rows (T=1 and T=32), one JSON line")
+    ap.add_argument("--rvq-rows", nargs="?", const="all", default=None, choices=("all", "rvq", "freq", "e8p"),
+                    help="profiling case: only the OLMoE-shaped VQ layer rows (T=1 and T=32) of one code or all, "
+                         "one JSON line")
     args = ap.parse_args()
     global CFG, T_MAIN, WORKLOAD
     if args.experts or args.tokens:
@@ -678,9 +702,10 @@ def main():
     if args.rvq_rows:
         if rank == 0:
             pk = hbm_peak()[0]
-            print(json.dumps({"workload": "olmoe-rvq rows (profiling case)",
-                              "rows": _rvq_rows(device, pk) + _rvq_rows(device, pk, synth.OLMOE_RVQ_FREQ) +
-                              _rvq_rows(device, pk, synth.OLMOE_E8P)}))
+            pick = {"rvq": [synth.OLMOE_RVQ], "freq": [synth.OLMOE_RVQ_FREQ], "e8p": [synth.OLMOE_E8P],
+                    "all": [synth.OLMOE_RVQ, synth.OLMOE_RVQ_FREQ, synth.OLMOE_E8P]}[args.rvq_rows]
+            print(json.dumps({"workload": "olmoe-shaped VQ layer rows (profiling case)",
+                              "rows": [r for c in pick for r in _rvq_rows(device, pk, c)]}))
         return 0
     t_setup = time.time()
     layer = build_dict_layer(CFG, device)
