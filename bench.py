@@ -383,6 +383,23 @@ def _dict_layer_row(layer, cfg, T, device, peak, note=""):
             "stream_bytes": sb, "stream_gbs": sb / t / 1e9, "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak}
 
 
+def _graph_time(step, n=50, warm=5):
+    """Time of `step` replayed from a CUDA graph (host launch overhead removed)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    t = _time_calls(graph.replay, n=n, warm=warm)
+    del graph
+    return t
+
+
 def _rvq_phases(call, K=20):
     """Device time of rvq_moe_layer's phases (library phase events), averaged over K calls."""
     import torch
@@ -444,6 +461,7 @@ def _rvq_rows(device, peak, cfg=None):
             Q.qmoe_route(lg, cfg.top_k, ids, gates)
             Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws, y_is_f32=False)
         t = _time_calls(step)
+        t_graph = _graph_time(step)
         phases = _rvq_phases(lambda: Q.rvq_moe_layer(sets[0], sets[1], sets[2], x, ids, gates, y, ws,
                                                      y_is_f32=False))
         touched = np.unique(ids.cpu().numpy().reshape(-1))
@@ -458,7 +476,8 @@ def _rvq_rows(device, peak, cfg=None):
                                 f"{label}), T={T}" + (" (tcgen05 path)" if T * cfg.top_k >= 16 else ""),
                     "tokens_per_s": T / t, "ms_per_call": t * 1e3, "touched_experts": int(len(touched)),
                     "stream_bytes": int(sb), "stream_gbs": sb / t / 1e9,
-                    "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak, "phase_ms": phases})
+                    "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak, "phase_ms": phases,
+                    "ms_per_call_cuda_graph": t_graph * 1e3})
     return out
 
 

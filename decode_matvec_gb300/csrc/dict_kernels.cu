@@ -640,17 +640,41 @@ __device__ __forceinline__ uint32_t u4_at(const uint4& v, int q) { return q == 0
 // of (row, block) into its row of the tile.  Codewords are read 16 at a time
 // as aligned 16-byte chunks, then all their compact entries, so that a block
 // costs a few memory round trips instead of two per codeword.
-__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, uint64_t lo, uint64_t hi,
+// The block's codeword range and its first 16-codeword window, loaded one block ahead (while the
+// previous block's MMAs run).  `ok` is false for a range no valid block can have (every codeword
+// covers at least two weights); then nothing is loaded.
+struct RowBlockAhead {
+    uint64_t lo, hi;
+    uint4 ch0, ch1;
+    bool ok;
+};
+
+__device__ __forceinline__ RowBlockAhead load_row_block(const uint16_t* codes, const uint32_t* off, uint64_t cbase,
+                                                        int row, int nb, int b, int blen) {
+    RowBlockAhead p;
+    p.lo = cbase + off[(size_t)row * nb + b];
+    p.hi = cbase + off[(size_t)row * nb + b + 1];
+    p.ok = !(p.hi < p.lo || p.hi - p.lo > (uint64_t)(blen / 2));
+    const uint64_t c8 = p.lo & ~7ull;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    p.ch0 = p.ok && c8 < p.hi ? __ldg((const uint4*)(codes + c8)) : z;
+    p.ch1 = p.ok && c8 + 8 < p.hi ? __ldg((const uint4*)(codes + c8 + 8)) : z;
+    return p;
+}
+
+__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, const RowBlockAhead& p,
                                                  int blen, unsigned char* A, int rl, bool& bad) {
     unsigned char* rowbase = A + (rl >> 3) * kDtcSBO + (rl & 7) * 16;
-    if (hi < lo || hi - lo > (uint64_t)(blen / 2)) {         // every codeword covers at least two weights
+    const uint64_t lo = p.lo, hi = p.hi;
+    if (!p.ok) {
         bad = true;
         return;
     }
     int col = 0;
     for (uint64_t c8 = lo & ~7ull; c8 < hi; c8 += 16) {
-        const uint4 ch0 = __ldg((const uint4*)(codes + c8));
-        const uint4 ch1 = c8 + 8 < hi ? __ldg((const uint4*)(codes + c8 + 8)) : make_uint4(0, 0, 0, 0);
+        const bool first = c8 == (lo & ~7ull);
+        const uint4 ch0 = first ? p.ch0 : __ldg((const uint4*)(codes + c8));
+        const uint4 ch1 = first ? p.ch1 : c8 + 8 < hi ? __ldg((const uint4*)(codes + c8 + 8)) : make_uint4(0, 0, 0, 0);
         uint32_t code[16], ea[16], eb[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -725,16 +749,19 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
         __syncthreads();
         const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
         const uint64_t cbase = m.code_base ? m.code_base[job.matrix] : 0ull;
+        const int drow = r0 + tid;                       // the row a decoding thread (tid < kDtcM) expands
+        const bool decodes = tid < kDtcM && drow < m.rows;
+        RowBlockAhead ahead{};
+        if (decodes) ahead = load_row_block(m.codes, off, cbase, drow, m.nb, 0, min(kDtcK, m.cols));
         for (int b = 0; b < m.nb; ++b) {
             const int blen = min(kDtcK, m.cols - b * kDtcK);
-            // zero the weight tile (16 bytes per store)
-            for (int i = tid; i < kDtcABytes / 16; i += kDtcThreads) ((uint4*)A)[i] = make_uint4(0, 0, 0, 0);
-            __syncthreads();
             if (tid < kDtcM) {
-                const int row = r0 + tid;
-                if (row < m.rows)
-                    decode_row_block(a, m.codes, cbase + off[(size_t)row * m.nb + b],
-                                     cbase + off[(size_t)row * m.nb + b + 1], blen, A, tid, bad);
+                // zero this thread's tile row (16 bytes per store; 8 consecutive rows fill a core
+                // matrix), then write its nonzeros
+                unsigned char* rowbase = A + (tid >> 3) * kDtcSBO + (tid & 7) * 16;
+#pragma unroll 8
+                for (int j = 0; j < kDtcK / 8; ++j) *(uint4*)(rowbase + j * kDtcLBO) = make_uint4(0, 0, 0, 0);
+                if (decodes) decode_row_block(a, m.codes, ahead, blen, A, tid, bad);
             } else {
                 // activations: 64 tokens x 256 columns in 16-byte asynchronous copies
                 // (zero-filled past the tokens and columns that exist), all in flight at once
@@ -762,6 +789,9 @@ __global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs 
                             umma_desc(b0 + k * 2 * kDtcLBO, kDtcLBO, kDtcSBO), kDtcIdesc, b > 0 || k > 0);
                 mma_commit(bar);
             }
+            // the next block's codeword range and first window, while the MMAs run
+            if (decodes && b + 1 < m.nb)
+                ahead = load_row_block(m.codes, off, cbase, drow, m.nb, b + 1, min(kDtcK, m.cols - (b + 1) * kDtcK));
             // the tiles are rewritten by the next block: wait for these MMAs
             if (!mbar_wait(bar, phase & 1u, kDtcSpin)) timed_out = true;
             ++phase;

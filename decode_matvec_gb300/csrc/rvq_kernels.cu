@@ -13,6 +13,7 @@
 // accumulated dot product once.  The Walsh-Hadamard transforms are in-shared-
 // memory butterflies (O(n log n)), one block per activation row.
 
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -256,6 +257,38 @@ __global__ void out_transform_kernel(const float* __restrict__ yp, const int32_t
     }
 }
 
+// The same output transform with the k slots of a token on the k CTAs of one thread-block cluster
+// (2 <= k <= 8): CTA j transforms slot j in its own shared memory and multiplies by D_out; after a
+// cluster barrier CTA j sums columns [j n / k, (j+1) n / k) over the slots in slot order, reading
+// the other CTAs' shared memory, with the per-element arithmetic of out_transform_kernel.
+__global__ void out_transform_cluster_kernel(const float* __restrict__ yp, const int32_t* __restrict__ expert_of,
+                                             const int8_t* __restrict__ so, const float* __restrict__ gates, int k,
+                                             int n, float norm, void* __restrict__ y, int y_is_f32) {
+    extern __shared__ float sm[];
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int j = (int)cluster.block_rank();
+    const int t = blockIdx.x / k;
+    const int slot = t * k + j;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) sm[i] = yp[(size_t)slot * n + i];
+    __syncthreads();
+    fwht_smem(sm, n, norm);
+    const int e = expert_of ? expert_of[slot] : 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) sm[i] = sm[i] * (float)so[(size_t)e * n + i];
+    cluster.sync();
+    const int c0 = (int)((long long)j * n / k), c1 = (int)((long long)(j + 1) * n / k);
+    for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+        float a = 0.0f;
+        for (int q = 0; q < k; ++q) {
+            const float* peer = cluster.map_shared_rank(sm, q);
+            a = fmaf(gates ? gates[t * k + q] : 1.0f, peer[i], a);
+        }
+        if (y_is_f32) ((float*)y)[(size_t)t * n + i] = a;
+        else ((uint16_t*)y)[(size_t)t * n + i] = f32_to_bf16(a);
+    }
+    cluster.sync();                                       // peers may still read this block's memory
+}
+
 // ---------------------------------------------------------------- decode-multiply (CUDA cores)
 struct RvqGemmArgs {
     RvqDev m;
@@ -294,7 +327,63 @@ __device__ __forceinline__ void decode_vec(const uint4* cb, const uint32_t (&cod
     }
 }
 
+// vectors a lane loads ahead: 8 (a whole row for cols <= 2048) for one token with one or two
+// stages, 2 for eight tokens, else 4 (the accumulators and codes share 128 registers)
+__host__ __device__ constexpr int rvq_batch(int nt, int s) { return nt == 1 && s < 3 ? 8 : nt == 8 ? 2 : 4; }
+
 // E8: the codes are E8P code words (S = 2 bytes each) and scb holds the staged E8P table.
+// The codes of kB vectors v0, v0 + 32, ... of one row (ip = the row's first code byte); 0 past nv.
+template <int S, bool E8, int kB>
+__device__ __forceinline__ void rvq_load_codes(const uint8_t* ip, int nv, int v0, uint32_t (&dst)[kB][E8 ? 1 : S]) {
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+        const int v = v0 + 32 * u;
+        if constexpr (E8 || S == 2) {
+            dst[u][0] = v < nv ? __ldg((const uint16_t*)ip + v) : 0u;
+        } else {
+#pragma unroll
+            for (int st = 0; st < S; ++st) dst[u][st] = v < nv ? __ldg(ip + (size_t)v * S + st) : 0u;
+        }
+    }
+}
+
+// One vector's 8 decoded weights from its loaded code word(s).
+template <int S, bool E8>
+__device__ __forceinline__ void rvq_decode_one(const uint4* scb, const uint32_t (&cw)[E8 ? 1 : S], int lane,
+                                               float (&w)[8]) {
+    if constexpr (E8) {
+        e8p_float8(((const uint2*)scb)[(cw[0] & 255u) * kE8pRepGemm + (lane & (kE8pRepGemm - 1))], cw[0], w);
+    } else {
+        uint32_t code[S];
+        if constexpr (S == 2) {
+            code[0] = cw[0] & 255u;
+            code[1] = cw[0] >> 8;
+        } else {
+#pragma unroll
+            for (int st = 0; st < S; ++st) code[st] = cw[st];
+        }
+        decode_vec<S>(scb, code, w);
+    }
+}
+
+// acc[t] += w . x_t over the vector's 8 columns (activations staged [token][column]).
+template <int NT>
+__device__ __forceinline__ void rvq_fma_tokens(const float* xs, int cols, int v, const float (&w)[8], float (&acc)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const float4* xt = (const float4*)(xs + (size_t)t * cols) + 2 * v;
+        const float4 x0 = xt[0], x1 = xt[1];
+        acc[t] = fmaf(w[0], x0.x, acc[t]);
+        acc[t] = fmaf(w[1], x0.y, acc[t]);
+        acc[t] = fmaf(w[2], x0.z, acc[t]);
+        acc[t] = fmaf(w[3], x0.w, acc[t]);
+        acc[t] = fmaf(w[4], x1.x, acc[t]);
+        acc[t] = fmaf(w[5], x1.y, acc[t]);
+        acc[t] = fmaf(w[6], x1.z, acc[t]);
+        acc[t] = fmaf(w[7], x1.w, acc[t]);
+    }
+}
+
 template <int NT, int S, bool E8 = false>
 __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const float* xs, const Job& job, int r0,
                               int warp, int nwarps, int lane) {
@@ -302,53 +391,37 @@ __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const floa
     const int nv = m.cols / 8;
     const int r1 = min(m.rows, r0 + a.rows_per_tile);
     const uint8_t* codes = codes_of(m, job.matrix);
+    const int row_bytes = nv * S;
     for (int r = r0 + warp; r < r1; r += nwarps) {
-        const uint8_t* ip = codes + (size_t)r * nv * S;
+        const uint8_t* ip = codes + (size_t)r * row_bytes;
+        // the warp's next row into L1 (a hint, no registers): its code loads then hit L1
+        if (r + nwarps < r1)
+            for (int l = lane * 128; l < row_bytes; l += 32 * 128)
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(ip + (size_t)nwarps * row_bytes + l));
         float acc[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
-        for (int v = lane; v < nv; v += 32) {
-            float w[8];
-            if constexpr (E8) {
-                const uint32_t cw = __ldg((const uint16_t*)ip + v);
-                e8p_float8(((const uint2*)scb)[(cw & 255u) * kE8pRepGemm + (lane & (kE8pRepGemm - 1))], cw, w);
-            } else {
-                uint32_t code[S];
-                if constexpr (S == 2) {
-                    const uint32_t pr = __ldg((const uint16_t*)ip + v);
-                    code[0] = pr & 255u;
-                    code[1] = pr >> 8;
+        // up to kRvqBatch vectors per lane: all their code loads are issued before the first decode
+        constexpr int kRvqBatch = rvq_batch(NT, S);
+        for (int v0 = lane; v0 < nv; v0 += 32 * kRvqBatch) {
+            uint32_t cwb[kRvqBatch][E8 ? 1 : S];
+#pragma unroll
+            for (int u = 0; u < kRvqBatch; ++u) {
+                const int v = v0 + 32 * u;
+                if constexpr (E8 || S == 2) {
+                    cwb[u][0] = v < nv ? __ldg((const uint16_t*)ip + v) : 0u;
                 } else {
 #pragma unroll
-                    for (int st = 0; st < S; ++st) code[st] = __ldg(ip + (size_t)v * S + st);
+                    for (int st = 0; st < S; ++st) cwb[u][st] = v < nv ? __ldg(ip + (size_t)v * S + st) : 0u;
                 }
-                decode_vec<S>(scb, code, w);
             }
-            if constexpr (NT == 1) {
-                const float4 x0 = ((const float4*)xs)[2 * v], x1 = ((const float4*)xs)[2 * v + 1];
-                acc[0] = fmaf(w[0], x0.x, acc[0]);
-                acc[0] = fmaf(w[1], x0.y, acc[0]);
-                acc[0] = fmaf(w[2], x0.z, acc[0]);
-                acc[0] = fmaf(w[3], x0.w, acc[0]);
-                acc[0] = fmaf(w[4], x1.x, acc[0]);
-                acc[0] = fmaf(w[5], x1.y, acc[0]);
-                acc[0] = fmaf(w[6], x1.z, acc[0]);
-                acc[0] = fmaf(w[7], x1.w, acc[0]);
-            } else {
-                // activations staged [token][column]: a lane's 8 columns are 32 contiguous bytes
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const float4* xt = (const float4*)(xs + (size_t)t * m.cols) + 2 * v;
-                    const float4 x0 = xt[0], x1 = xt[1];
-                    acc[t] = fmaf(w[0], x0.x, acc[t]);
-                    acc[t] = fmaf(w[1], x0.y, acc[t]);
-                    acc[t] = fmaf(w[2], x0.z, acc[t]);
-                    acc[t] = fmaf(w[3], x0.w, acc[t]);
-                    acc[t] = fmaf(w[4], x1.x, acc[t]);
-                    acc[t] = fmaf(w[5], x1.y, acc[t]);
-                    acc[t] = fmaf(w[6], x1.z, acc[t]);
-                    acc[t] = fmaf(w[7], x1.w, acc[t]);
-                }
+            for (int u = 0; u < kRvqBatch; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= nv) break;
+                float w[8];
+                rvq_decode_one<S, E8>(scb, cwb[u], lane, w);
+                rvq_fma_tokens<NT>(xs, m.cols, v, w, acc);
             }
         }
         const float s = f16_to_f32(m.scale[(size_t)job.matrix * m.rows + r]);
@@ -603,13 +676,15 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
             job.n_tok = min(kTcN, a.T_implicit - j * kTcN);
         }
         const int r0 = (tile % a.row_tiles) * kTcM;
-        // per thread: A part (row, half of a chunk's 16 vectors), B part (token, two 8-wide K groups)
-        const int rl = tid >> 1, part = tid & 1;
+        // per thread: A part (row, half of a chunk's 16 vectors), B part (token, two 8-wide K groups);
+        // the 8 lanes of a quarter-warp take 8 consecutive rows (tokens), so their 16-byte tile stores
+        // fill one 128-byte core matrix: no shared-memory bank conflict
+        const int rl = (tid & 7) | ((tid >> 4) << 3), part = (tid >> 3) & 1;
         const int arow = r0 + rl;
         const int S = stages_of(m, job.matrix);              // code bytes per vector (8-byte aligned runs of kTcVpt)
         if (S == 0) continue;                                 // uniform over the block: skip the tile
         const uint8_t* ip = codes_of(m, job.matrix) + ((size_t)(arow < m.rows ? arow : 0) * nv + part * kTcVpt) * S;
-        const int bn = tid >> 3, bg = tid & 7;
+        const int bn = (tid & 7) | ((tid >> 6) << 3), bg = (tid >> 3) & 7;
         const int bslot = bn < job.n_tok ? (a.slots ? a.slots[job.slot_begin + bn] : job.slot_begin + bn) : -1;
         const float* bp = a.xr + (size_t)(bslot < 0 ? 0 : bslot) * m.cols + bg * 16;
         // the global loads of chunk kc + 1 are issued before chunk kc is decoded
@@ -829,6 +904,26 @@ int fwht_threads(int n) { return std::min(512, std::max(32, n / 2)); }
 // Output transform of T tokens with k slots each (slot outputs yp [T*k][n]).
 int launch_out_transform(const float* yp, const int32_t* expert_of, const int8_t* so, const float* gates, int T,
                          int k, int n, void* y, int y_is_f32, cudaStream_t st) {
+    if (k >= 2 && k <= 8) {
+        // one block per slot, the slots of a token in one cluster
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(T * k));
+        cfg.blockDim = dim3((unsigned)fwht_threads(n));
+        cfg.dynamicSmemBytes = (size_t)n * sizeof(float);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)k;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int rc = qmoe::cuda_check(cudaLaunchKernelEx(&cfg, out_transform_cluster_kernel, yp, expert_of, so, gates, k,
+                                                     n, inv_sqrt(n), y, y_is_f32),
+                                  "out transform (cluster) launch");
+        if (rc) return rc;
+        return qmoe::launch_check("out_transform_cluster_kernel");
+    }
     const int kg = std::max(1, std::min(k, 98304 / (4 * n) - 1));
     const size_t smem = (size_t)(kg + 1) * n * sizeof(float);
     int rc = qmoe::cuda_check(cudaFuncSetAttribute(out_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
