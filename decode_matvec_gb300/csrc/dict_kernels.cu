@@ -932,6 +932,60 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
     }
 }
 
+// The same router for E <= 256: a lane keeps its (up to) 8 logits and a taken mask in registers,
+// and lane j keeps the j-th choice, so the k passes read the logits once and use no local memory.
+// Selection, tie-breaking and gates are those of route_kernel.
+__global__ void route_kernel_small(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                                   float* __restrict__ gates) {
+    const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float* row = logits + (size_t)t * E;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = lane + 32 * i < E ? row[lane + 32 * i] : -INFINITY;
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_v = 0.0f, first_v = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(QMOE_FULL_MASK, bv, d);
+            const int oi = __shfl_xor_sync(QMOE_FULL_MASK, bi, d);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane && bi < E) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_id = bi;
+            my_v = bv;
+        }
+        if (j == 0) first_v = bv;
+    }
+    const float mx = first_v;
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i < E) sum += expf(v[i] - mx);
+    sum = warp_sum(sum);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = my_id;
+        gates[(size_t)t * k + lane] = expf(my_v - mx) / sum;
+    }
+}
+
 // ------------------------------------------------------------ planner
 // One block: histogram, exclusive scan, stable placement (one warp, in slot
 // order) and the job tables of both matrices of the layer.
@@ -1249,7 +1303,8 @@ extern "C" int qmoe_route(const float* logits, int T, int E, int k, int32_t* ids
     if (!logits || !ids || !gates) return fail(QMOE_EINVAL, "qmoe_route: NULL pointer");
     const int threads = 256;
     const long long blocks = ((long long)T * 32 + threads - 1) / threads;
-    route_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
+    if (E <= 256) route_kernel_small<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
+    else route_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
     return qmoe::launch_check("qmoe_route");
 }
 

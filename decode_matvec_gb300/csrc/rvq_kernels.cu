@@ -97,9 +97,27 @@ __device__ __forceinline__ uint2 e8p_bytes(uint32_t w) {
     return make_uint2(lo, hi);
 }
 
-// table[p * rep + r] = pattern p's bytes, r = 0 .. rep-1.  Every thread of the block calls it.
-__device__ __forceinline__ void e8p_stage_table(const uint32_t* __restrict__ g, uint2* t, int rep) {
-    for (int i = threadIdx.x; i < 256 * rep; i += blockDim.x) t[i] = e8p_bytes(__ldg(g + i / rep));
+// table[p * kRep + r] = pattern p's bytes, r = 0 .. kRep-1, by a block of kThreads threads (all
+// call it); the loads are issued together.
+template <int kRep, int kThreads>
+__device__ __forceinline__ void e8p_stage_table(const uint32_t* __restrict__ g, uint2* t) {
+    constexpr int kPer = 256 * kRep / kThreads;
+    static_assert(kPer * kThreads == 256 * kRep, "table entries per thread");
+    uint32_t w[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) w[j] = __ldg(g + (threadIdx.x + j * kThreads) / kRep);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) t[threadIdx.x + j * kThreads] = e8p_bytes(w[j]);
+}
+
+// Codebooks [n_st][256] x 16 bytes into shared memory by 256 threads, the loads issued together.
+__device__ __forceinline__ void rvq_stage_codebooks(const uint4* __restrict__ g, uint4* t, int n_st) {
+    uint4 c[QMOE_RVQ_MAX_STAGES];
+#pragma unroll
+    for (int j = 0; j < QMOE_RVQ_MAX_STAGES; ++j) c[j] = j < n_st ? __ldg(g + threadIdx.x + j * 256) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < QMOE_RVQ_MAX_STAGES; ++j)
+        if (j < n_st) t[threadIdx.x + j * 256] = c[j];
 }
 
 __device__ __forceinline__ void e8p_half8(uint2 pb, uint32_t code, uint32_t (&h)[4]) {
@@ -181,6 +199,7 @@ __global__ void in_transform_kernel(const uint16_t* __restrict__ x, int x_div, c
     const uint16_t* src = x + (size_t)(row / x_div) * n;
     float* s0 = sm;
     float* s1 = sm + n;
+#pragma unroll 4
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         const float v = bf16_to_f32(src[i]);
         s0[i] = v * (float)si0[(size_t)e * n + i];
@@ -206,6 +225,7 @@ __global__ void swiglu_transform_kernel(const float* __restrict__ gp, const floa
     const int e = expert_of[row];
     float* sg = sm;
     float* su = sm + n;
+#pragma unroll 4
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         sg[i] = gp[(size_t)row * n + i];
         su[i] = up[(size_t)row * n + i];
@@ -270,6 +290,7 @@ __global__ void out_transform_cluster_kernel(const float* __restrict__ yp, const
     const int j = (int)cluster.block_rank();
     const int t = blockIdx.x / k;
     const int slot = t * k + j;
+#pragma unroll 4
     for (int i = threadIdx.x; i < n; i += blockDim.x) sm[i] = yp[(size_t)slot * n + i];
     __syncthreads();
     fwht_smem(sm, n, norm);
@@ -391,13 +412,8 @@ __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const floa
     const int nv = m.cols / 8;
     const int r1 = min(m.rows, r0 + a.rows_per_tile);
     const uint8_t* codes = codes_of(m, job.matrix);
-    const int row_bytes = nv * S;
     for (int r = r0 + warp; r < r1; r += nwarps) {
-        const uint8_t* ip = codes + (size_t)r * row_bytes;
-        // the warp's next row into L1 (a hint, no registers): its code loads then hit L1
-        if (r + nwarps < r1)
-            for (int l = lane * 128; l < row_bytes; l += 32 * 128)
-                asm volatile("prefetch.global.L1 [%0];" ::"l"(ip + (size_t)nwarps * row_bytes + l));
+        const uint8_t* ip = codes + (size_t)r * nv * S;
         float acc[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
@@ -438,16 +454,26 @@ __device__ void rvq_tile_rows(const RvqGemmArgs& a, const uint4* scb, const floa
 
 constexpr int kRvqThreads = 256;
 
+// The job's activation rows [token][column] into shared memory (zeros past its tokens); rows are
+// copied as float4, two per thread at a time with the loads issued together (a 2048-column row
+// in one round trip).
 template <int NT>
 __device__ void rvq_stage(const RvqGemmArgs& a, const Job& job, float* xs) {
-    const int cols = a.m.cols;
+    const int n4 = a.m.cols / 4;
     for (int t = 0; t < NT; ++t) {
-        if (t < job.n_tok) {
-            const int slot = a.slots ? a.slots[job.slot_begin + t] : job.slot_begin + t;
-            const float* src = a.xr + (size_t)slot * cols;
-            for (int c = threadIdx.x; c < cols; c += blockDim.x) xs[(size_t)t * cols + c] = src[c];
-        } else {
-            for (int c = threadIdx.x; c < cols; c += blockDim.x) xs[(size_t)t * cols + c] = 0.0f;
+        const int slot = t >= job.n_tok ? -1 : a.slots ? a.slots[job.slot_begin + t] : job.slot_begin + t;
+        const float4* src = (const float4*)(a.xr + (size_t)(slot < 0 ? 0 : slot) * a.m.cols);
+        float4* dst = (float4*)(xs + (size_t)t * a.m.cols);
+        for (int c0 = threadIdx.x; c0 < n4; c0 += 2 * blockDim.x) {
+            float4 v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int c = c0 + u * blockDim.x;
+                v[u] = slot >= 0 && c < n4 ? src[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (c0 + u * blockDim.x < n4) dst[c0 + u * blockDim.x] = v[u];
         }
     }
 }
@@ -458,9 +484,8 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq_gemm_kernel(const RvqGemmA
     uint4* scb = (uint4*)smem;                  // [n_st][256] x 8 fp16, or the replicated E8P table
     float* xs = (float*)(smem + (a.m.e8p ? (size_t)256 * kE8pRepGemm * 8 : (size_t)a.m.n_st * 256 * 16));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    if (a.m.e8p) e8p_stage_table((const uint32_t*)a.m.cb, (uint2*)smem, kE8pRepGemm);
-    else
-        for (int i = tid; i < a.m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)a.m.cb + i);
+    if (a.m.e8p) e8p_stage_table<kE8pRepGemm, kRvqThreads>((const uint32_t*)a.m.cb, (uint2*)smem);
+    else rvq_stage_codebooks((const uint4*)a.m.cb, scb, a.m.n_st);
     __syncthreads();
     const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + a.nt_max - 1) / a.nt_max;
     const int n_tiles = n_jobs * a.row_tiles;
@@ -637,9 +662,8 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const RvqDev& m = a.m;
 
-    if (m.e8p) e8p_stage_table((const uint32_t*)m.cb, (uint2*)scb, kE8pRepTc);
-    else
-        for (int i = tid; i < m.n_st * 256; i += blockDim.x) scb[i] = __ldg((const uint4*)m.cb + i);
+    if (m.e8p) e8p_stage_table<kE8pRepTc, kTcThreads>((const uint32_t*)m.cb, (uint2*)scb);
+    else rvq_stage_codebooks((const uint4*)m.cb, scb, m.n_st);
     if (tid == 0) {
         for (int b = 0; b < 2; ++b)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + b)) : "memory");
