@@ -887,7 +887,9 @@ __global__ void decode_dense_kernel(const uint32_t* __restrict__ words, MatDev m
 }
 
 // ------------------------------------------------------------ router
-__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+// Router for E > 256 and many tokens: one warp per token (more tokens per block than
+// route_kernel_block); the chosen experts are kept in a per-thread array.
+__global__ void route_kernel_warp(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
                              float* __restrict__ gates) {
     const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
@@ -898,11 +900,13 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int bi = 0x7FFFFFFF;
+        // loads first and unconditional, eight iterations unrolled: the loads go out together
+#pragma unroll 8
         for (int e = lane; e < E; e += 32) {
+            const float v = row[e];
             bool taken = false;
             for (int q = 0; q < j; ++q) taken |= (chosen[q] == e);
             if (taken) continue;
-            const float v = row[e];
             if (v > bv || (v == bv && e < bi)) {
                 bv = v;
                 bi = e;
@@ -922,6 +926,7 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
     }
     const float mx = chosen_v[0];
     float sum = 0.0f;
+#pragma unroll 8
     for (int e = lane; e < E; e += 32) sum += expf(row[e] - mx);
     sum = warp_sum(sum);
     if (lane == 0) {
@@ -932,9 +937,91 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
     }
 }
 
-// The same router for E <= 256: a lane keeps its (up to) 8 logits and a taken mask in registers,
-// and lane j keeps the j-th choice, so the k passes read the logits once and use no local memory.
-// Selection, tie-breaking and gates are those of route_kernel.
+// Router for 256 < E <= 8192: one block of 256 threads per token; thread i keeps logits
+// i, i + 256, ... (up to 32) and a taken mask in registers; each of the k passes is a block-wide
+// argmax (highest logit, ties to the lower expert id).  Gates: softmax over all E logits read at
+// the chosen experts.
+constexpr int kRouteBlock = 256;
+// up to this many tokens a block per token (latency); beyond, a warp per token (throughput)
+constexpr int kRouteBlockMaxT = 512;
+
+__global__ void __launch_bounds__(kRouteBlock) route_kernel_block(const float* __restrict__ logits, int T, int E,
+                                                                  int k, int32_t* __restrict__ ids,
+                                                                  float* __restrict__ gates) {
+    __shared__ float wv[kRouteBlock / 32], s_v[32], s_sum[kRouteBlock / 32];
+    __shared__ int wi[kRouteBlock / 32], s_id[32];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* row = logits + (size_t)t * E;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = tid + kRouteBlock * i < E ? row[tid + kRouteBlock * i] : -INFINITY;
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int e = tid + kRouteBlock * i;
+            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(QMOE_FULL_MASK, bv, d);
+            const int oi = __shfl_xor_sync(QMOE_FULL_MASK, bi, d);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == 0) {
+            wv[warp] = bv;
+            wi[warp] = bi;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            bv = lane < kRouteBlock / 32 ? wv[lane] : -INFINITY;
+            bi = lane < kRouteBlock / 32 ? wi[lane] : 0x7FFFFFFF;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const float ov = __shfl_xor_sync(QMOE_FULL_MASK, bv, d);
+                const int oi = __shfl_xor_sync(QMOE_FULL_MASK, bi, d);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (lane == 0) {
+                s_v[j] = bv;
+                s_id[j] = bi;
+            }
+        }
+        __syncthreads();
+        const int c = s_id[j];
+        if (c < E && (c % kRouteBlock) == tid) taken |= 1u << (c / kRouteBlock);
+    }
+    const float mx = s_v[0];
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (tid + kRouteBlock * i < E) sum += expf(v[i] - mx);
+    sum = warp_sum(sum);
+    if (lane == 0) s_sum[warp] = sum;
+    __syncthreads();
+    if (warp == 0) {
+        const float tot = warp_sum(lane < kRouteBlock / 32 ? s_sum[lane] : 0.0f);
+        if (lane < k) {
+            ids[(size_t)t * k + lane] = s_id[lane];
+            gates[(size_t)t * k + lane] = expf(s_v[lane] - mx) / tot;
+        }
+    }
+}
+
+// Router for E <= 256: one warp per token; a lane keeps its (up to) 8 logits and a taken mask in
+// registers, and lane j keeps the j-th choice.  Same selection, tie-breaking and gates as
+// route_kernel_block.
 __global__ void route_kernel_small(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
                                    float* __restrict__ gates) {
     const int t = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
@@ -1014,11 +1101,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
                                                             int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                                             Job* __restrict__ jobs_a, Job* __restrict__ jobs_b,
                                                             Job* __restrict__ jobs_tc, int* __restrict__ n_jobs) {
-    __shared__ int hist[kPlanMaxE];
+    // shared memory: hist[E] (counts, then running positions) and off[E + 1] (exclusive offsets);
+    // thread i owns experts [i per, (i + 1) per), so one block scan covers all E
+    extern __shared__ int psm[];
+    int* hist = psm;
+    int* off = psm + E;
     __shared__ int sbuf[32];
-    __shared__ int carry;
     const int tid = threadIdx.x;
-    for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    for (int e = e0; e < e1; ++e) hist[e] = 0;
     __syncthreads();
     for (int i = tid; i < n_slots; i += blockDim.x) {
         const int e = ids[i];
@@ -1026,26 +1118,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         else atomicAdd(&hist[e], 1);
     }
     __syncthreads();
-    // exclusive scan of hist in chunks of blockDim
-    if (tid == 0) carry = 0;
-    __syncthreads();
-    for (int base = 0; base < E; base += blockDim.x) {
-        const int e = base + tid;
-        const int c = e < E ? hist[e] : 0;
-        const int ex = block_excl_scan(c, sbuf);
-        if (e < E) {
-            counts[e] = c;
-            offsets[e] = carry + ex;
-        }
-        __syncthreads();
-        if (tid == blockDim.x - 1) carry += ex + c;
-        __syncthreads();
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += hist[e];
+    const int ex = block_excl_scan(local, sbuf);
+    int run = ex;
+    for (int e = e0; e < e1; ++e) {
+        const int c = hist[e];
+        counts[e] = c;
+        offsets[e] = run;
+        off[e] = run;
+        hist[e] = run;                                 // running position for the placement
+        run += c;
     }
-    if (tid == 0) offsets[E] = carry;
+    if (tid == blockDim.x - 1) {
+        offsets[E] = ex + local;
+        off[E] = ex + local;
+    }
     __syncthreads();
     // stable placement: warp 0 walks the slots in order
-    for (int e = tid; e < E; e += blockDim.x) hist[e] = offsets[e];
-    __syncthreads();
     if (tid < 32) {
         const int lane = tid;
         for (int base = 0; base < n_slots; base += 32) {
@@ -1065,10 +1155,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             __syncwarp();
         }
     }
-    __syncthreads();
     if (!jobs_a) return;
     // job tables in expert order: chunks of nt tokens of the experts each kernel takes
-    // (experts with at least tc_min tokens go to the tensor-core kernel when tc_min > 0)
+    // (experts with at least tc_min tokens go to the tensor-core kernel when tc_min > 0); counts
+    // and offsets come from shared memory
     for (int which = 0; which < 3; ++which) {
         const int nt = which == 0 ? nt_a : which == 1 ? nt_b : nt_tc;
         Job* jobs = which == 0 ? jobs_a : which == 1 ? jobs_b : jobs_tc;
@@ -1076,30 +1166,32 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
             if (tid == 0) n_jobs[2] = 0;
             break;
         }
-        if (tid == 0) carry = 0;
-        __syncthreads();
-        for (int base = 0; base < E; base += blockDim.x) {
-            const int e = base + tid;
-            int c = e < E ? counts[e] : 0;
+        int nj_local = 0;
+        for (int e = e0; e < e1; ++e) {
+            int c = off[e + 1] - off[e];
+            const bool tc = tc_min > 0 && c >= tc_min;
+            if (tc != (which == 2)) c = 0;
+            nj_local += (c + nt - 1) / nt;
+        }
+        const int first0 = block_excl_scan(nj_local, sbuf);
+        int first = first0;
+        for (int e = e0; e < e1; ++e) {
+            int c = off[e + 1] - off[e];
             const bool tc = tc_min > 0 && c >= tc_min;
             if (tc != (which == 2)) c = 0;
             const int nj = (c + nt - 1) / nt;
-            const int ex = block_excl_scan(nj, sbuf);
-            const int first = carry + ex;
             for (int q = 0; q < nj; ++q) {
                 Job jb;
                 jb.matrix = e;
-                jb.slot_begin = offsets[e] + q * nt;
+                jb.slot_begin = off[e] + q * nt;
                 jb.n_tok = min(nt, c - q * nt);
                 jb.pad = 0;
                 jobs[first + q] = jb;
             }
-            __syncthreads();
-            if (tid == blockDim.x - 1) carry += ex + nj;
-            __syncthreads();
+            first += nj;
         }
-        if (tid == 0) n_jobs[which] = carry;
-        __syncthreads();
+        if (tid == blockDim.x - 1) n_jobs[which] = first0 + nj_local;
+        __syncthreads();                               // sbuf is reused by the next scan
     }
 }
 
@@ -1230,8 +1322,14 @@ int sm_count() {
 int launch_plan(const int32_t* ids, int n_slots, int E, int nt_a, int nt_b, int32_t* counts, int32_t* offsets,
                 int32_t* perm, Job* jobs_a, Job* jobs_b, int* n_jobs, cudaStream_t st, int tc_min, int nt_tc,
                 Job* jobs_tc) {
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(ids, n_slots, E, nt_a, nt_b, tc_min, nt_tc, counts, offsets, perm, jobs_a,
-                                            jobs_b, jobs_tc, n_jobs);
+    const size_t smem = (size_t)(2 * E + 1) * sizeof(int);
+    if (smem > 48 * 1024) {
+        const int rc = cuda_check(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                                  "plan attr");
+        if (rc) return rc;
+    }
+    plan_kernel<<<1, kPlanThreads, smem, st>>>(ids, n_slots, E, nt_a, nt_b, tc_min, nt_tc, counts, offsets, perm, jobs_a,
+                                               jobs_b, jobs_tc, n_jobs);
     return launch_check("plan_kernel");
 }
 
@@ -1304,7 +1402,9 @@ extern "C" int qmoe_route(const float* logits, int T, int E, int k, int32_t* ids
     const int threads = 256;
     const long long blocks = ((long long)T * 32 + threads - 1) / threads;
     if (E <= 256) route_kernel_small<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
-    else route_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
+    else if (T <= kRouteBlockMaxT)
+        route_kernel_block<<<(unsigned)T, kRouteBlock, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
+    else route_kernel_warp<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(logits, T, E, k, ids, gates);
     return qmoe::launch_check("qmoe_route");
 }
 

@@ -152,8 +152,11 @@ def test_bad_arguments_rejected_on_host(dev, dict886):
         Q.qmoe_expert_matvec(dict886, bad, bf16_tensor(synth.activations_bf16(1, 1, 64)), y)
 
 
-@pytest.mark.parametrize("T,E,k", [(64, 128, 1), (37, 64, 8), (5, 7, 3)])
+@pytest.mark.parametrize("T,E,k", [(64, 128, 1), (37, 64, 8), (5, 7, 3), (1, 64, 8), (3, 256, 32),
+                                   (33, 2048, 1), (9, 300, 4), (2, 257, 32), (600, 300, 4)])
 def test_route_parity(dev, T, E, k):
+    """E <= 256: a warp per token with the logits in registers; larger E: a block per token up to
+    512 tokens, a warp per token beyond."""
     lg = synth.zipf_logits(4, T, E, 0.9)
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     gates = torch.empty((T, k), dtype=torch.float32, device=dev)
@@ -163,9 +166,11 @@ def test_route_parity(dev, T, E, k):
     assert np.allclose(gates.cpu().numpy(), rg, rtol=1e-5, atol=1e-7)
 
 
-def test_route_ties_go_to_lower_id(dev):
-    lg = np.zeros((3, 40), np.float32)
+@pytest.mark.parametrize("E", [40, 600])
+def test_route_ties_go_to_lower_id(dev, E):
+    lg = np.zeros((3, E), np.float32)
     lg[1, [5, 9, 30]] = 2.0
+    lg[2, [E - 1, 3, 33]] = -1.0
     ids = torch.empty((3, 4), dtype=torch.int32, device=dev)
     gates = torch.empty((3, 4), dtype=torch.float32, device=dev)
     Q.qmoe_route(torch.from_numpy(lg).to(dev), 4, ids, gates)
