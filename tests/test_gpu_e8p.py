@@ -140,8 +140,10 @@ def _layer(dev, gate, up, down, E, d, f, T, k, seed, sample=None):
 
 
 @pytest.mark.parametrize("E,d,f,T,k", [(8, 256, 128, 20, 4), (16, 512, 256, 32, 8), (4, 128, 64, 1, 2),
-                                       (6, 256, 512, 40, 2), (5, 128, 256, 7, 3)])
+                                       (6, 256, 512, 40, 2), (5, 128, 256, 7, 3), (12, 128, 256, 3, 10),
+                                       (16, 256, 128, 2, 12)])
 def test_e8p_moe_layer_parity(dev, E, d, f, T, k):
+    """k <= 8: the output transform runs on a thread-block cluster per token; k > 8 on one block."""
     seed = 37
     gate = [_random(seed, e, synth.GATE, f, d) for e in range(E)]
     up = [_random(seed, e, synth.UP, f, d) for e in range(E)]
