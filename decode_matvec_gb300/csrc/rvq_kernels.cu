@@ -11,7 +11,16 @@
 // C1[i1] + C2[i2] in registers from shared-memory codebooks and multiplies it
 // into the staged rotated activations; the row scale multiplies the
 // accumulated dot product once.  The Walsh-Hadamard transforms are in-shared-
-// memory butterflies (O(n log n)), one block per activation row.
+// memory butterflies (O(n log n)), one block per activation row (the output
+// transform: one block per slot, the slots of a token on one cluster).
+//
+// The same kernels run the E8P lattice code ("M8.5 - Extreme Weight
+// Compression and Representations", 0x06E) when the matrix set's format says
+// so: one 16-bit code word per 8 weights, decoded from a 256-entry table of
+// absolute patterns with explicit signs, a parity-implied last sign and a
+// +-1/4 shift (see e8p_half8).  Frequency-conditioned sets give each matrix
+// 1 to 3 residual stages ("Quantization as Cache Amplification",
+// Frequency-Conditioned Bit Allocation).
 
 #include <cooperative_groups.h>
 #include <cuda_fp16.h>
@@ -84,7 +93,7 @@ bool valid_set(const rvq_matrix_set* s) {
 // sign bits are spread onto the two halves' sign bits with one multiply, and
 // one fp16x2 add applies the +-1/4 shift.  Every coordinate is a multiple of
 // 1/4 below 3, so every step is exact.
-constexpr int kE8pRepGemm = 16;   // table replicas in rvq_gemm_kernel (8-byte entries: 16 banks pairs)
+constexpr int kE8pRepGemm = 16;   // table replicas in rvq_gemm_kernel (8-byte entries: 16 bank pairs)
 constexpr int kE8pRepTc = 4;      // table replicas in rvq_tc_kernel
 
 __device__ __forceinline__ uint2 e8p_bytes(uint32_t w) {
