@@ -297,6 +297,41 @@ def time_e2e(step, K, W):
 
 
 # ---------------------------------------------------------------- CPU oracle timing
+def sampled_parity(step, cfg, tokens):
+    """The timed layer call again with fp32 output; for a few sampled tokens, the normwise relative
+    error against the float64 oracle layer computed from the seeded ternary weights and row scales
+    themselves (so dictionary, encoder, decoder and product are all checked)."""
+    import torch
+    from oracle import moe as M
+    from oracle import products as P
+    Q, L = step.Q, step.layer
+    y32 = torch.empty((step.T, L.d_model), dtype=torch.float32, device=step.x.device)
+    Q.qmoe_route(step.logits, 1, step.ids, step.gates)
+    Q.qmoe_moe_layer(L.dictionary, L.wi, L.wo, step.x, step.ids, step.gates, y32, step.ws, y_is_f32=True)
+    status = Q.qmoe_check_status()
+    y = y32.cpu().numpy()
+    rid, rg = M.route(step.logits_host, 1)
+    x = synth.bf16_to_f64(step.x_host)
+    lib = native_synth()                     # the seeded ternary generator (checked against synth's definition)
+    thr = synth.zero_threshold(cfg.p0)
+    worst = 0.0
+    for t in tokens:
+        e = int(rid[t, 0])
+        w = []
+        for m in (synth.WI, synth.WO):
+            rows, cols = synth.dict_matrix_shape(cfg, m)
+            tern = np.zeros((rows, cols), np.int8)
+            lib.synth_ternary_rows(cfg.seed, e, m, cols, thr, 0, rows, tern.ctypes.data)
+            s = synth.row_scales(cfg.seed, e, m, rows).view(np.float16).astype(np.float64)
+            w.append(tern.astype(np.float64) * s[:, None])
+        ref = rg[t, 0] * M.relu_expert(x[t:t + 1], w[0], w[1])[0]
+        worst = max(worst, P.normwise_rel_err(y[t], ref))
+    return {"max_normwise_rel_err": worst, "tolerance": 2e-3, "status_ok": status == Q.QMOE_OK,
+            "routing_equal": bool(np.array_equal(step.ids.cpu().numpy(), rid)),
+            "sample": f"tokens {list(tokens)}: fp32-mode output against the float64 oracle from the seeded "
+                      "ternary weights (max |y - ref| / max |ref| per token)"}
+
+
 class OracleSampler:
     """Times the CPU oracle on bounded samples of the layer: decode + float64 product of a
     64-row slice of one touched expert's matrix for that expert's tokens.  Inputs are
@@ -772,6 +807,10 @@ def main():
                    "parallelism": f"{world} independent replicas (one token batch per GPU)"},
         "stream_gbs": stream_bytes / (secs / args.steps) / 1e9,
         "stream_pct_of_hbm_peak": 100.0 * stream_bytes / (secs / args.steps) / 1e9 / peak,
+        # the dense bf16 bytes of the touched experts' weights the step replaces, per second; and the
+        # stored bits per weight of those experts (codes, block offsets, row scales)
+        "decoded_weight_gbs": len(touched) * 2 * CFG.d_model * CFG.d_ff * 2 / (secs / args.steps) / 1e9,
+        "effective_bits_per_weight": 8.0 * stream_bytes / (len(touched) * 2 * CFG.d_model * CFG.d_ff),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_kind": "measured (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": achieved / peak,
@@ -784,6 +823,7 @@ def main():
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = OracleSampler(CFG, T_MAIN).run(budget_s=6.0 if args.quick else 20.0)
+        line["parity"] = sampled_parity(step, CFG, (0, T_MAIN // 2, T_MAIN - 1))
     if rank == 0 and not args.quick:
         line["rows"] = extra_rows(layer, device, peak)
     if rank == 0:
