@@ -221,15 +221,20 @@ def time_steps(step, K, W, world):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(K):
+    # one event between consecutive steps: the first and last bracket the K steps, the others give
+    # the per-step distribution
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev[0].record(st)
+    for i in range(K):
         step.run()
-    e1.record(st)
+        ev[i + 1].record(st)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / 1000.0
+    per = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(K)])
+    time_steps.distribution_ms = {"p10": float(np.percentile(per, 10)), "p50": float(np.percentile(per, 50)),
+                                  "p90": float(np.percentile(per, 90))}
+    return ev[0].elapsed_time(ev[K]) / 1000.0
 
 
 def time_phases(step, K):
@@ -800,6 +805,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "ms_per_step_distribution": getattr(time_steps, "distribution_ms", None),
         "config": {"workload": WORKLOAD, "tokens": T_MAIN, "activations": "bf16 in/out, fp32 accumulate",
                    "touched_experts": int(len(touched)),
                    "l2": "inputs larger than L2: each step streams the touched experts' compressed weights "
