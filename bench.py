@@ -214,6 +214,7 @@ class DictStep:
 
 
 def time_steps(step, K, W, world):
+    """K timed steps after W warm-up steps, bracketed by barriers; returns (seconds, {p10, p50, p90} ms)."""
     import torch
     st = torch.cuda.current_stream()
     for _ in range(W):
@@ -232,9 +233,8 @@ def time_steps(step, K, W, world):
     barrier(world)
     torch.cuda.synchronize()
     per = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(K)])
-    time_steps.distribution_ms = {"p10": float(np.percentile(per, 10)), "p50": float(np.percentile(per, 50)),
-                                  "p90": float(np.percentile(per, 90))}
-    return ev[0].elapsed_time(ev[K]) / 1000.0
+    dist = {q: float(np.percentile(per, v)) for q, v in (("p10", 10), ("p50", 50), ("p90", 90))}
+    return ev[0].elapsed_time(ev[K]) / 1000.0, dist
 
 
 def time_phases(step, K):
@@ -774,7 +774,7 @@ def main():
     step = DictStep(layer, CFG, T_MAIN, rank, device)
 
     with ClockSampler(local if world > 1 else 0) as clk:
-        secs = time_steps(step, args.steps, args.warmup, world)
+        secs, step_dist = time_steps(step, args.steps, args.warmup, world)
     secs = max_over_ranks(secs, world)
     ms_per_step = secs / args.steps * 1e3
     value = T_MAIN * world / (secs / args.steps)
@@ -805,7 +805,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "ms_per_step_distribution": getattr(time_steps, "distribution_ms", None),
+        "ms_per_step_distribution": step_dist,
         "config": {"workload": WORKLOAD, "tokens": T_MAIN, "activations": "bf16 in/out, fp32 accumulate",
                    "touched_experts": int(len(touched)),
                    "l2": "inputs larger than L2: each step streams the touched experts' compressed weights "
