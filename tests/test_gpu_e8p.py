@@ -183,3 +183,40 @@ def test_e8p_bad_sets_rejected(dev):
             Q.rvq_expert_matmul(s, xb, y, ws)
         s = _set([mt], rows, cols)
     assert Q.qmoe_check_status() == Q.QMOE_OK
+
+
+@pytest.mark.parametrize("T", [3, 24])
+def test_mixed_formats_in_one_layer(dev, T):
+    """Each matrix set carries its own format: E8P gate and down with a two-stage RVQ up matrix."""
+    E, d, f, k, seed = 6, 256, 128, 2, 41
+    gate = [_random(seed, e, synth.GATE, f, d) for e in range(E)]
+    down = [_random(seed, e, synth.DOWN, d, f) for e in range(E)]
+    rng = np.random.default_rng(seed)
+    cb = R.f16_round(rng.standard_normal((2, 256, 8)) * 0.5)
+    cb_bits = cb.astype(np.float16).view(np.uint16)
+    up = []
+    for e in range(E):
+        idx = rng.integers(0, 256, (f, d // 8, 2)).astype(np.uint8)
+        sc = (rng.uniform(0.5, 1.5, f) * 0.02).astype(np.float16).view(np.uint16)
+        so, si = synth.rvq_signs(seed, e, synth.UP, f, d)
+        up.append(dict(idx=idx, scale=sc, so=so, si=si))
+    su = Q.RvqMatrixSet.from_host(np.stack([m["idx"] for m in up]), cb_bits, np.concatenate([m["scale"] for m in up]),
+                                  np.concatenate([m["so"] for m in up]), np.concatenate([m["si"] for m in up]), E, f, d)
+    sg, sd = _set(gate, f, d), _set(down, d, f)
+    lg = synth.zipf_logits(seed, T, E, 0.9)
+    xb = synth.activations_bf16(seed, T, d)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+    Q.qmoe_route(torch.from_numpy(lg).to(dev), k, ids, gates)
+    ws = torch.empty(Q.rvq_moe_layer_ws_size(E, d, f, T, k), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    Q.rvq_moe_layer(sg, su, sd, bf16_tensor(xb), ids, gates, y, ws)
+    assert Q.qmoe_check_status() == Q.QMOE_OK
+    rid, rg = M.route(lg, k)
+
+    def expert(e, xs):
+        u = (R.decode(up[e]["idx"], cb_bits, up[e]["scale"]), up[e]["so"], up[e]["si"])
+        return R.swiglu_expert(xs, _triple(gate[e]), u, _triple(down[e]))
+
+    ref = M.moe_layer(synth.bf16_to_f64(xb), rid, rg, expert, d)
+    assert P.normwise_rel_err(y.cpu().numpy(), ref) < TOL
