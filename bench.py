@@ -274,30 +274,58 @@ def time_phases(step, K):
 
 
 def time_e2e(step, K, W):
-    """Same step through the public API with host buffers: H2D inputs, compute, D2H output, each step."""
+    """The same step through the public API with host buffers, pipelined the way a serving loop runs
+    it: step i's inputs (x, router logits) go host -> device on one copy stream while step i - 1
+    computes, and step i - 1's output goes device -> host on another; inputs and outputs are double
+    buffered.  Every step's copies are inside the timed region."""
     import torch
+    Q, L = step.Q, step.layer
     x_pin = torch.from_numpy(step.x_host.view(np.int16).copy()).pin_memory()
     lg_pin = torch.from_numpy(step.logits_host).pin_memory()
-    y_pin = torch.empty(tuple(step.y.shape), dtype=torch.int16).pin_memory()
-    st = torch.cuda.current_stream()
+    comp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    bufs = [dict(x=torch.empty_like(step.x), lg=torch.empty_like(step.logits), y=torch.empty_like(step.y),
+                 y_pin=torch.empty(tuple(step.y.shape), dtype=torch.int16).pin_memory()) for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    for s_ in range(2):
+        computed[s_].record(comp)
+        out_done[s_].record(comp)
 
-    def one():
-        step.x.copy_(x_pin, non_blocking=True)
-        step.logits.copy_(lg_pin, non_blocking=True)
-        step.run()
-        y_pin.copy_(step.y, non_blocking=True)
+    def issue(i):
+        s_ = i % 2
+        b = bufs[s_]
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(computed[s_])             # step i - 2 has finished reading these inputs
+            b["x"].copy_(x_pin, non_blocking=True)
+            b["lg"].copy_(lg_pin, non_blocking=True)
+            in_ready[s_].record(h2d)
+        comp.wait_event(in_ready[s_])
+        comp.wait_event(out_done[s_])                # step i - 2's output has been copied out
+        Q.qmoe_route(b["lg"], 1, step.ids, step.gates, stream=comp)
+        Q.qmoe_moe_layer(L.dictionary, L.wi, L.wo, b["x"], step.ids, step.gates, b["y"], step.ws, y_is_f32=False,
+                         stream=comp)
+        computed[s_].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(computed[s_])
+            b["y_pin"].copy_(b["y"], non_blocking=True)
+            out_done[s_].record(d2h)
 
-    for _ in range(W):
-        one()
+    for i in range(W):
+        issue(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(K):
-        one()
-    e1.record(st)
+    e0.record(comp)
+    h2d.wait_event(e0)
+    d2h.wait_event(e0)
+    for i in range(K):
+        issue(i)
+    comp.wait_event(out_done[(K - 1) % 2])
+    e1.record(comp)
     torch.cuda.synchronize()
     bi = x_pin.numel() * 2 + lg_pin.numel() * 4
-    bo = y_pin.numel() * 2
+    bo = bufs[0]["y_pin"].numel() * 2
     return e0.elapsed_time(e1) / 1000.0 / K, bi, bo
 
 
