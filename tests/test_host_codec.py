@@ -217,3 +217,19 @@ def test_e8p_pack_codewords_round_trip():
     got, sc = Q.e8p_pack(w, so, si)
     want, wsc = P8.encode(R.rotate_weight(w, so, si))
     assert np.array_equal(sc, wsc) and np.array_equal(got, want)
+
+
+def test_e8p_pack_rejects_bad_inputs():
+    w = synth.rvq_weight(4, 0, 0, 16, 64)
+    so, si = synth.rvq_signs(4, 0, 0, 16, 64)
+    with pytest.raises(Q.QmoeError):
+        Q.e8p_pack(w[:, :48], so, si[:48])                  # 48 columns: not a power of two
+    with pytest.raises(Q.QmoeError):
+        Q.e8p_pack(w[:12], so[:12], si)                     # 12 rows: not a power of two
+    bad = si.copy()
+    bad[3] = 0
+    with pytest.raises(Q.QmoeError):
+        Q.e8p_pack(w, so, bad)                              # a sign that is not +-1
+    with pytest.raises(Q.QmoeError):
+        Q.e8p_pack(np.zeros((16, 64)), so, si)             # a zero row has no scale
+    assert Q.e8p_nearest(np.zeros((0, 8))).shape == (0,)
