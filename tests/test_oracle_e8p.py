@@ -183,3 +183,18 @@ def test_scale_and_encode_of_a_rotated_weight():
                                .astype(np.float32)))
     rel = np.linalg.norm(wd - wr) / np.linalg.norm(wr)
     assert 0.2 < rel < 0.35
+
+
+def test_codewords_keep_the_e8_minimal_distance():
+    """E8 has minimal squared norm 2, so distinct points of E8 + 1/4 are at squared distance >= 2,
+    with equality for neighbours; a wrong parity rule or shift would bring codewords closer."""
+    cb = P.codebook()
+    rng = np.random.default_rng(13)
+    pick = rng.choice(65536, 300, replace=False)
+    best = np.inf
+    for c in pick:
+        d = ((cb - cb[c]) ** 2).sum(axis=1)
+        d[c] = np.inf
+        best = min(best, float(d.min()))
+        assert d.min() >= 2.0
+    assert best == 2.0
