@@ -177,7 +177,7 @@ def test_route_ties_go_to_lower_id(dev, E):
     assert ids.cpu().numpy().tolist() == M.route(lg, 4)[0].tolist()
 
 
-@pytest.mark.parametrize("T,k,E", [(512, 1, 128), (40, 8, 64), (4096, 1, 2048), (1, 1, 5)])
+@pytest.mark.parametrize("T,k,E", [(512, 1, 128), (40, 8, 64), (4096, 1, 2048), (1, 1, 5), (300, 2, 8192)])
 def test_bucketise_exact(dev, T, k, E):
     ids_np = M.route(synth.zipf_logits(3, T, E, 1.0), k)[0]
     ids = torch.from_numpy(ids_np).to(dev)
