@@ -21,7 +21,7 @@ SYNTH_SRC = os.path.join(ROOT, "synth", "csrc", "synth.cpp")
 SYNTH_LIB = os.path.join(ROOT, "synth", "libsynth.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["dict_kernels.cu", "rvq_kernels.cu", "tc_kernels.cu", "pack_kernels.cu"]
+CU_SOURCES = ["dict_kernels.cu", "rvq_kernels.cu", "pack_kernels.cu"]
 CPP_SOURCES = ["host_codec.cpp"]
 
 

@@ -139,3 +139,34 @@ def test_ledger_counts_everything():
     assert math.isclose(led["effective_bits_per_weight"], 8 * (2000 + 324 + 20) / 20000)
     assert math.isclose(led["effective_with_dictionary"], led["effective_bits_per_weight"] + 8 * 524288 / 20000)
     assert math.isclose(led["bitmask_bits_per_weight"], 1.1)
+
+
+def test_ledger_of_a_hand_counted_artifact(words886):
+    # [M8.5] 0x01A / 0x08A: the effective rate counts every stored byte.  A 2 x 512 all-zero matrix in
+    # 256-weight blocks: each block is nine 28-zero runs and one 4-zero run (greedy longest match
+    # over the 14 all-zero entries), so 2 rows x 2 blocks x 10 = 40 codewords = 80 bytes; block
+    # offsets 2 x 2 + 1 = 5 uint32 = 20 bytes; row scales 2 fp16 = 4 bytes; 1024 weights.
+    tern = np.zeros((2, 512), np.int8)
+    words86 = words886
+    codes, off = C.encode(tern, words86)
+    scales = np.array([0x2000, 0x2400], np.uint16)
+    assert len(codes) == 40 and codes.nbytes == 80 and off.nbytes == 20 and scales.nbytes == 4
+    led = C.ledger(len(codes), 2, 512, off.nbytes, scales.nbytes)
+    assert led["payload_bits_per_weight"] == 16 * 40 / 1024                  # 0.625
+    assert led["effective_bits_per_weight"] == 8 * (80 + 20 + 4) / 1024      # 0.8125
+    # the shared dictionary: 2^16 entries x two uint32 words = 524,288 bytes
+    assert words86.nbytes == 524288
+    assert led["effective_with_dictionary"] == 8 * (80 + 20 + 4 + 524288) / 1024
+    assert led["compression_vs_bf16"] == 16 / 0.8125
+    assert led["mean_run"] == 1024 / 40
+
+
+def test_ledger_one_nonzero_per_block(words886):
+    # one +1 at the start of each block: a 28-run with one nonzero, then eight 28-zero runs and a
+    # 4-zero run, again 10 codewords per block; one row of 768 weights = 3 blocks = 30 codewords.
+    tern = np.zeros((1, 768), np.int8)
+    tern[0, [0, 256, 512]] = 1
+    codes, off = C.encode(tern, words886)
+    assert len(codes) == 30 and off.nbytes == 16
+    led = C.ledger(len(codes), 1, 768, off.nbytes, 2)
+    assert led["effective_bits_per_weight"] == 8 * (60 + 16 + 2) / 768

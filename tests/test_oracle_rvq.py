@@ -1,4 +1,6 @@
 """Pins for the oracle's randomized Hadamard transform and residual VQ."""
+import math
+
 import numpy as np
 import pytest
 
@@ -196,3 +198,63 @@ def test_encode_prefix_consistency_across_stage_counts():
         d = R.decode(idx, R.f16_round(cb3).astype(np.float16).view(np.uint16), R.row_scale_f16(wr))
         errs.append(float(np.sum((d - wr) ** 2)))
     assert errs[0] > errs[1] > errs[2]
+
+
+# ---------------------------------------------------------------- pins of the expert FFN and the row scale
+def _h2():
+    """The 2 x 2 normalised Hadamard matrix written out (independent of the oracle's builder)."""
+    r = 1.0 / math.sqrt(2.0)
+    return np.array([[r, r], [r, -r]])
+
+
+def _rotated(w, sign_out, sign_in):
+    """W' = H D_out W D_in H for 2 x 2 matrices, so that the transform-aware product gives W x."""
+    h = _h2()
+    return h @ np.diag(sign_out) @ np.asarray(w, np.float64) @ np.diag(sign_in) @ h
+
+
+def test_swiglu_expert_hand_computed():
+    # [QCA] expert FFN (SwiGLU): y = down(bf16(SiLU(gate x) * (up x))).  Plain weights
+    # gate = I, up = [[0, 1], [1, 0]], down = [[1, 1], [1, -1]], x = (1, 2):
+    #   g = (1, 2), u = (2, 1)
+    #   SiLU(1) * 2 = 2 / (1 + e^-1) = 1.46211715726...  -> bf16 1 + 59/128 = 1.4609375
+    #   SiLU(2) * 1 = 2 / (1 + e^-2) = 1.76159415595...  -> bf16 1 + 97/128 = 1.7578125
+    #   y = (1.4609375 + 1.7578125, 1.4609375 - 1.7578125) = (3.21875, -0.296875)
+    # Swapping gate and up gives y[1] = +0.296875; dropping the bf16 rounding of h gives
+    # (3.22371131..., -0.29947699...).
+    so, si = np.array([1.0, -1.0]), np.array([-1.0, -1.0])
+    gate = (_rotated(np.eye(2), so, si), so, si)
+    up = (_rotated([[0, 1], [1, 0]], so[::-1].copy(), si), so[::-1].copy(), si)
+    down = (_rotated([[1, 1], [1, -1]], si, so), si, so)
+    y = R.swiglu_expert(np.array([[1.0, 2.0]]), gate, up, down)
+    assert np.allclose(y, [[3.21875, -0.296875]], rtol=0, atol=1e-12)
+
+
+def test_swiglu_expert_one_dimensional():
+    # one-dimensional layers (the 1 x 1 Hadamard is 1) with unit weights: SiLU(0) * u = 0, and
+    # for x = 1, h = SiLU(1) * 1 = 0.73105857... rounds to the nearest bf16, 187/256 (spacing
+    # 2^-8 on [0.5, 1); 187.15 units); down = 1 passes h through.
+    one = (np.ones((1, 1)), np.ones(1), np.ones(1))
+    assert R.swiglu_expert(np.array([[0.0]]), one, one, one)[0, 0] == 0.0
+    assert R.swiglu_expert(np.array([[1.0]]), one, one, one)[0, 0] == 187.0 / 256.0
+    # x = -1: h = SiLU(-1) * (-1) = 0.26894142... -> 0.26953125 (138/512, spacing 2^-9)
+    assert R.swiglu_expert(np.array([[-1.0]]), one, one, one)[0, 0] == 138.0 / 512.0
+
+
+@pytest.mark.parametrize("row,expected", [
+    # a constant row c: RMS = |c|
+    ([0.02] * 16, np.float16(0.02)),
+    ([-0.375] * 8, np.float16(0.375)),
+    # (a, -a, 0, 0): RMS = |a| / sqrt(2)
+    ([0.5, -0.5, 0.0, 0.0], np.float16(0.5 / math.sqrt(2.0))),
+    # (3, 4) / (5 * sqrt(2)) scaled: RMS of (3, 4) is 5 / sqrt(2)
+    ([3.0, 4.0], np.float16(5.0 / math.sqrt(2.0))),
+    # one nonzero among n = 8: RMS = |v| / sqrt(8)
+    ([0.0, 0.0, 0.0, 0.1, 0.0, 0.0, 0.0, 0.0], np.float16(0.1 / math.sqrt(8.0))),
+])
+def test_row_scale_f16_closed_forms(row, expected):
+    # [QCA] "Residual vector quantization": per-row RMS scale, stored in fp16.  A scale of
+    # max|w|, or a root of the sum without the division by n, fails every row but the first.
+    got = R.row_scale_f16(np.array([row]))
+    assert got.dtype == np.uint16
+    assert got[0] == np.array([expected], np.float16).view(np.uint16)[0]
