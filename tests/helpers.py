@@ -55,3 +55,43 @@ def bf16_tensor(bits: np.ndarray, device="cuda"):
 def bf16_values(t) -> np.ndarray:
     """Device bf16 (int16 view) -> float64 host values."""
     return synth.bf16_to_f64(t.cpu().numpy().view(np.uint16))
+
+
+@functools.lru_cache(maxsize=1)
+def _native_synth():
+    import ctypes
+    import os
+    lib = ctypes.CDLL(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "synth",
+                                   "libsynth.so"))
+    lib.synth_ternary_rows.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int64,
+                                       ctypes.c_uint32, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    lib.synth_ternary_rows.restype = None
+    return lib
+
+
+def fill_ternary(seed, expert, matrix, p0, out):
+    """Fill int8 out[rows, cols] with synth.ternary_rows(...) through the native twin of the generator
+    (same numbers; the twin is checked against the Python definition in test_host_codec)."""
+    rows, cols = out.shape
+    _native_synth().synth_ternary_rows(seed, expert, matrix, cols, synth.zero_threshold(p0), 0, rows,
+                                       out.ctypes.data)
+    return out
+
+
+def seeded_weights(seed, expert, matrix, rows, cols, p0):
+    """float64 weights s_r * t_rc of one seeded ternary matrix (the oracle's definition of the layer)."""
+    tern = fill_ternary(seed, expert, matrix, p0, np.empty((rows, cols), np.int8))
+    s = synth.f16_to_f64(synth.row_scales(seed, expert, matrix, rows))
+    return tern.astype(np.float64) * s[:, None]
+
+
+def rvq_oracle_matrix(args):
+    """Oracle-coded RVQ matrix (decoded W', sign_out, sign_in) of one seeded expert matrix: rotate,
+    encode with the given fp16 codebooks, decode.  A plain function so that a spawn pool can run it."""
+    from oracle import rvq as R
+    seed, e, m, rows, cols, cb_bits = args
+    w = synth.rvq_weight(seed, e, m, rows, cols)
+    so, si = synth.rvq_signs(seed, e, m, rows, cols)
+    cb = np.asarray(cb_bits, np.uint16).view(np.float16).astype(np.float64)
+    idx, sc = R.encode(R.rotate_weight(w, so, si), cb)
+    return R.decode(idx, cb_bits, sc), so, si
