@@ -754,6 +754,8 @@ def main():
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling case: keep only this many experts of the c2048-shaped layer")
     ap.add_argument("--tokens", type=int, default=None, help="profiling case: token batch size")
+    ap.add_argument("--dict-rows", action="store_true",
+                    help="profiling case: only the switch-base-128 / switch-large-128 layer rows, one JSON line")
     ap.add_argument("--rvq-rows", nargs="?", const="all", default=None, choices=("all", "rvq", "freq", "e8p"),
                     help="profiling case: only the OLMoE-shaped VQ layer rows (T=1 and T=32) of one code or all, "
                          "one JSON line")
@@ -788,6 +790,18 @@ def main():
     import torch
     device = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(device)
+    if args.dict_rows:
+        if rank == 0:
+            pk = hbm_peak()[0]
+            rows = []
+            for cfg in (synth.SWITCH_BASE_128, synth.SWITCH_LARGE_128):
+                small = build_dict_layer(cfg, device)
+                rows += [_dict_layer_row(small, cfg, T, device, pk, " (layer fits in L2: not an HBM figure)")
+                         for T in cfg.tokens]
+                del small
+            print(json.dumps({"workload": "switch-base-128 / switch-large-128 layer rows (profiling case)",
+                              "rows": rows}))
+        return 0
     if args.rvq_rows:
         if rank == 0:
             pk = hbm_peak()[0]

@@ -187,37 +187,62 @@ __device__ __forceinline__ void lookup(const GemmArgs& a, const SmemMap& sm, uin
     }
 }
 
-// Adds one codeword's weights (at most three nonzeros, from the compact
-// slots) times the staged activations to the per-token sums; the run starts
-// at column cj.  Empty slots read nothing and add zero.
-template <int NT>
+// The compact slots of one entry: three 6-bit slots, or (ESC, flag 0x40) four
+// 4-bit slots of an entry with four nonzeros in its first eight positions.
+// Entries read through their canonical words have every slot empty (63).
+template <bool ESC>
+__device__ __forceinline__ void entry_slots(uint32_t ea, uint32_t eb, uint32_t (&sl)[4]) {
+    if constexpr (ESC) {
+        const bool four = (eb & 0x40u) != 0u;
+        sl[0] = four ? (ea >> 4) & 15u : (ea >> 4) & 63u;
+        sl[1] = four ? (ea >> 8) & 15u : ea >> 10;
+        sl[2] = four ? ea >> 12 : eb & 63u;
+        sl[3] = four ? eb & 15u : 63u;
+    } else {
+        sl[0] = (ea >> 4) & 63u;
+        sl[1] = ea >> 10;
+        sl[2] = eb & 63u;
+        sl[3] = 63u;
+    }
+}
+
+// Adds one codeword's weights (at most three nonzeros, four with ESC, from the
+// compact slots) times the staged activations to the per-token sums; the run
+// starts at column cj.  Empty slots read nothing and add zero.
+template <int NT, bool ESC>
 __device__ __forceinline__ void code_acc(uint32_t ea, uint32_t eb, int cj, uint32_t xs, float (&acc)[NT]) {
-    const uint32_t s0 = (ea >> 4) & 63u, s1 = ea >> 10, s2 = eb & 63u;
+    constexpr int NS = ESC ? 4 : 3;
+    uint32_t sl[4];
+    entry_slots<ESC>(ea, eb, sl);
     if constexpr (NT == 1) {
         const uint32_t base = xs + 4u * (uint32_t)cj;
-        uint32_t r0 = 0, r1 = 0, r2 = 0;
-        if (s0 != 63u) r0 = *(const uint16_t*)(g_smem + base + 2u * s0);
-        if (s1 != 63u) r1 = *(const uint16_t*)(g_smem + base + 2u * s1);
-        if (s2 != 63u) r2 = *(const uint16_t*)(g_smem + base + 2u * s2);
-        acc[0] = acc_add_lo(acc_add_lo(acc_add_lo(acc[0], r0), r1), r2);
+        uint32_t r[NS];
+#pragma unroll
+        for (int z = 0; z < NS; ++z) r[z] = sl[z] != 63u ? (uint32_t)*(const uint16_t*)(g_smem + base + 2u * sl[z]) : 0u;
+#pragma unroll
+        for (int z = 0; z < NS; ++z) acc[0] = acc_add_lo(acc[0], r[z]);
     } else {
         constexpr int W = NT / 2;
-        uint32_t w0[W], w1[W], w2[W];
+        uint32_t w[NS][W];
 #pragma unroll
-        for (int q = 0; q < W; ++q) w0[q] = w1[q] = w2[q] = 0u;
-        if (s0 != 63u) load_x<NT>(xs, cj + (int)(s0 >> 1), w0);
-        if (s1 != 63u) load_x<NT>(xs, cj + (int)(s1 >> 1), w1);
-        if (s2 != 63u) load_x<NT>(xs, cj + (int)(s2 >> 1), w2);
-        const uint32_t g0 = slot_sign(s0), g1 = slot_sign(s1), g2 = slot_sign(s2);
+        for (int z = 0; z < NS; ++z) {
 #pragma unroll
-        for (int q = 0; q < W; ++q) {
-            acc[2 * q] = acc_fma_lo(acc_fma_lo(acc_fma_lo(acc[2 * q], w0[q], g0), w1[q], g1), w2[q], g2);
-            acc[2 * q + 1] = acc_fma_hi(acc_fma_hi(acc_fma_hi(acc[2 * q + 1], w0[q], g0), w1[q], g1), w2[q], g2);
+            for (int q = 0; q < W; ++q) w[z][q] = 0u;
+            if (sl[z] != 63u) load_x<NT>(xs, cj + (int)(sl[z] >> 1), w[z]);
+        }
+#pragma unroll
+        for (int z = 0; z < NS; ++z) {
+            const uint32_t g = slot_sign(sl[z]);
+#pragma unroll
+            for (int q = 0; q < W; ++q) {
+                acc[2 * q] = acc_fma_lo(acc[2 * q], w[z][q], g);
+                acc[2 * q + 1] = acc_fma_hi(acc[2 * q + 1], w[z][q], g);
+            }
         }
     }
 }
 
-// Entry with more than three nonzeros (its compact slots are all empty): add
+// Entry outside the compact slots (flag 0x80; its slots are all empty): add
 // its weights from the canonical words.
 template <int NT>
 __device__ void escape_dot(const GemmArgs& a, uint32_t code, int len, int cj, uint32_t xs, float (&t)[NT]) {
@@ -251,6 +276,25 @@ template <int CPL>
 __device__ __forceinline__ uint4 load_codes(const uint16_t* p) {
     if constexpr (CPL == 8) return __ldg((const uint4*)p);
     else return make_uint4((uint32_t)__ldg(p), 0u, 0u, 0u);
+}
+
+// Accumulates a lane's CPL codewords: `total` over all of them, `lo` over those
+// that start in the lane's first row (a prefix: codewords are in stream order).
+template <int NT, int CPL, bool ESC>
+__device__ __forceinline__ void acc_codes(const uint32_t (&ea)[CPL], const uint32_t (&eb)[CPL], int col, int cols,
+                                          int cross, uint32_t xs, float (&total)[NT], float (&lo)[NT]) {
+    int pre = 0;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const bool second = pre >= cross;
+        const int cj = second ? col + pre - cols : col + pre;
+        code_acc<NT, ESC>(ea[j], eb[j], cj, xs, total);
+        if (!second) {
+#pragma unroll
+            for (int z = 0; z < NT; ++z) lo[z] = total[z];
+        }
+        pre += (int)(ea[j] & 15u) * 2;
+    }
 }
 
 // One window: CPL consecutive codewords per lane starting at stream index
@@ -289,25 +333,20 @@ __device__ __forceinline__ void window(const GemmArgs& a, const SmemMap& sm, uin
     float total[NT], lo[NT];
 #pragma unroll
     for (int z = 0; z < NT; ++z) total[z] = lo[z] = 0.0f;
-    int pre = 0;
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        const bool second = pre >= cross;
-        const int cj = second ? col + pre - cols : col + pre;
-        code_acc<NT>(ea[j], eb[j], cj, sm.xs, total);
-        if (!second) {
-#pragma unroll
-            for (int z = 0; z < NT; ++z) lo[z] = total[z];
-        }
-        pre += (int)(ea[j] & 15u) * 2;
-    }
-    if (esc & 64u) {
-        // rare: entries with more than three nonzeros, taken from the canonical words
+    // windows holding an entry with four nonzeros (flag 0x40; dictionaries for p0 below ~0.88)
+    // take the four-slot accumulation, the others the three-slot one
+    if (__any_sync(QMOE_FULL_MASK, esc & 0x40u))
+        acc_codes<NT, CPL, true>(ea, eb, col, cols, cross, sm.xs, total, lo);
+    else
+        acc_codes<NT, CPL, false>(ea, eb, col, cols, cross, sm.xs, total, lo);
+    if (esc & 0x80u) {
+        // entries outside the compact slots (five or more nonzeros, or a fourth one past the
+        // eighth position): taken from the canonical words
         int p2 = 0;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
             const int len = (int)(ea[j] & 15u) * 2;
-            if (eb[j] & 64u) {
+            if (eb[j] & 0x80u) {
                 const bool second = p2 >= cross;
                 const int cj = second ? col + p2 - cols : col + p2;
                 float t[NT];
@@ -698,7 +737,7 @@ __device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16
                 bad = true;
                 break;
             }
-            if (eb[k] & 64u) {
+            if (eb[k] & 0x80u) {
                 const uint32_t c0 = __ldg(a.words + 2 * code[k]), c1 = __ldg(a.words + 2 * code[k] + 1);
                 for (int q = 0; q < len; ++q) {
                     const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
@@ -708,9 +747,10 @@ __device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16
                     }
                 }
             } else {
-                const uint32_t sl[3] = {(ea[k] >> 4) & 63u, ea[k] >> 10, eb[k] & 63u};
+                uint32_t sl[4];
+                entry_slots<true>(ea[k], eb[k], sl);
 #pragma unroll
-                for (int z = 0; z < 3; ++z) {
+                for (int z = 0; z < 4; ++z) {
                     if (sl[z] != 63u) {
                         const int c = col + (int)(sl[z] >> 1);
                         *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) =

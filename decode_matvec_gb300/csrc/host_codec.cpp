@@ -246,10 +246,14 @@ extern "C" int qmoe_pack(const int8_t* tern, int rows, int cols, int block,
 }
 
 // ---------------------------------------------------------------------------
-// Compact dictionary: uint16 plane [65536] then uint8 plane [65536]
-//   plane A: [3:0] pair count, [9:4] slot 0, [15:10] slot 1
-//   plane B: [5:0] slot 2, [6] escape (more than three nonzeros)
-//   slot = 2*position + (1 if the weight is w_min), 63 = empty
+// Compact dictionary: uint16 plane [65536] then uint8 plane [65536];
+// slot = 2*position + (1 if the weight is w_min).
+//   up to three nonzeros:      A [3:0] pair count, [9:4] slot 0, [15:10] slot 1 (63 = empty)
+//                              B [5:0] slot 2 (63 = empty), [7:6] = 0
+//   four nonzeros, all in the  A [3:0] pair count, [7:4] slot 0, [11:8] slot 1, [15:12] slot 2
+//   first eight positions:     B [3:0] slot 3, [6] = 1 (four 4-bit slots), [7] = 0
+//   anything else:             A [3:0] pair count, [15:4] = 0xFFF; B = 0xBF ([7] = 1: the kernels
+//                              read the entry's canonical words)
 // ---------------------------------------------------------------------------
 extern "C" int qmoe_dict_compact(const uint32_t* dict_words, void* compact) {
     qmoe::clear_error();
@@ -261,7 +265,7 @@ extern "C" int qmoe_dict_compact(const uint32_t* dict_words, void* compact) {
         uint32_t pairs = w0 & 15u;
         if ((w1 & 15u) != pairs || pairs < 1 || pairs > 14)
             return fail(QMOE_EFORMAT, "qmoe_dict_compact: bad pair count");
-        int slots[3] = {63, 63, 63};
+        int slots[4] = {63, 63, 63, 63};
         int nnz = 0;
         for (int i = 0; i < 28; ++i) {
             uint32_t s = ((i < 14 ? w0 : w1) >> (4 + 2 * (i % 14))) & 3u;
@@ -271,14 +275,21 @@ extern "C" int qmoe_dict_compact(const uint32_t* dict_words, void* compact) {
                 continue;
             }
             if (s) {
-                if (nnz < 3) slots[nnz] = 2 * i + (s == 1 ? 1 : 0);
+                if (nnz < 4) slots[nnz] = 2 * i + (s == 1 ? 1 : 0);
                 ++nnz;
             }
         }
-        uint32_t esc = nnz > 3 ? 1u : 0u;
-        if (esc) slots[0] = slots[1] = slots[2] = 63;
-        pa[e] = (uint16_t)(pairs | ((uint32_t)slots[0] << 4) | ((uint32_t)slots[1] << 10));
-        pb[e] = (uint8_t)((uint32_t)slots[2] | (esc << 6));
+        if (nnz <= 3) {
+            pa[e] = (uint16_t)(pairs | ((uint32_t)slots[0] << 4) | ((uint32_t)slots[1] << 10));
+            pb[e] = (uint8_t)slots[2];
+        } else if (nnz == 4 && slots[3] < 16) {
+            pa[e] = (uint16_t)(pairs | ((uint32_t)slots[0] << 4) | ((uint32_t)slots[1] << 8) |
+                               ((uint32_t)slots[2] << 12));
+            pb[e] = (uint8_t)(slots[3] | 0x40);
+        } else {
+            pa[e] = (uint16_t)(pairs | 0xFFF0u);
+            pb[e] = 0xBF;
+        }
     }
     return QMOE_OK;
 }

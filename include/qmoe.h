@@ -126,9 +126,12 @@ int qmoe_pack(const int8_t* tern, int rows, int cols, int block,
 /*
  * Derive the kernel-private compact dictionary from the canonical entries.
  * The compact table holds, per entry, the pair count and the positions and
- * signs of up to three nonzero weights (24 bits: a uint16 plane followed by
- * a uint8 plane); entries with more than three nonzeros carry an escape flag
- * and the kernels read their canonical words instead.  Upload the result
+ * signs of its nonzero weights in 24 bits (a uint16 plane followed by a
+ * uint8 plane): three 6-bit slots for entries with up to three nonzeros,
+ * four 4-bit slots (and a flag) for entries with four nonzeros all in their
+ * first eight positions (the four-nonzero entries of dictionaries for
+ * p0 >= 0.8); any other entry carries a flag that sends the kernels to its
+ * canonical words.  Upload the result
  * next to the canonical words and point qmoe_dict.compact at it.
  *  dict_words host in, QMOE_DICT_WORDS uint32.
  *  compact   host out, QMOE_COMPACT_BYTES bytes.
@@ -344,7 +347,12 @@ int rvq_expert_matmul_ws_size(int rows, int cols, int T, size_t* bytes);
  * y[t] = D_out H (W' (H D_in x_t)) for one RVQ-coded matrix (count == 1):
  * input transform, fused codebook decode + multiply (CUDA cores for T < 16,
  * tcgen05 tensor cores with fp16 operands and fp32 accumulation for
- * T >= 16), output transform.
+ * T >= 16), output transform.  On the tensor-core path each rotated
+ * activation row is first multiplied by a power of two that brings its
+ * largest magnitude into [2^14, 2^15) (undone exactly in the epilogue), then
+ * split into an fp16 high part and the fp16 of the remainder; any finite bf16
+ * input stays inside fp16's range, and values below 2^-25 of their row's
+ * largest one are the only ones that lose low bits.
  *  x_bf16 device bf16 [T][cols];  y device [T][rows] fp32 or bf16.
  * Errors: EINVAL, ECAPACITY, ECUDA.
  */

@@ -79,19 +79,22 @@ def test_expert_matvec_parity(dev, dict886, T):
     assert np.array_equal(yb.cpu().numpy().view(np.uint16), synth.bf16_bits_from_f32(y.cpu().numpy()))
 
 
-def test_expert_matvec_escape_entries(dev, dict857):
-    # p0 = 0.857 dictionaries hold entries with four nonzeros (read through the escape path)
+@pytest.mark.parametrize("p0,most", [(0.857, 4), (0.75, 5)])
+def test_expert_matvec_escape_entries(dev, p0, most):
+    # p0 = 0.857 dictionaries hold entries with four nonzeros (the four-slot compact form); p0 = 0.75
+    # ones also entries with five (read through their canonical words)
+    d = Q.Dictionary(dictionary(p0))
     rows, cols = 64, 3072
-    tern, codes, off, scale = oracle_matrix(6, 0, 1, rows, cols, 0.857)
-    L, sym = C.expansion(dictionary(0.857))
+    tern, codes, off, scale = oracle_matrix(6, 0, 1, rows, cols, p0)
+    L, sym = C.expansion(dictionary(p0))
     nnz = (sym != 0).sum(axis=1)
-    assert (nnz[codes] > 3).any()
+    assert nnz[codes].max() == most
     m = _single(codes, off, scale, rows, cols)
-    for T in (1, 4, 7):
+    W = C.decode(codes, off, dictionary(p0), scale, rows, cols)
+    for T in (1, 2, 4, 7):
         xb = synth.activations_bf16(6, T, cols)
         y = torch.empty((T, rows), dtype=torch.float32, device=dev)
-        Q.qmoe_expert_matvec(dict857, m, bf16_tensor(xb), y)
-        W = C.decode(codes, off, dictionary(0.857), scale, rows, cols)
+        Q.qmoe_expert_matvec(d, m, bf16_tensor(xb), y)
         assert P.normwise_rel_err(y.cpu().numpy(), P.matmul_xwt(synth.bf16_to_f64(xb), W)) < 1e-5
     assert Q.qmoe_check_status() == Q.QMOE_OK
 
@@ -206,7 +209,9 @@ def _layer(E, d, f, p0, seed):
                                            # ~75 tensor-core jobs: 4-tile (wi) and 2-tile (wo) work items
                                            (2, 512, 1024, 4700, 1, 0.886),
                                            # 3-tile (wi) work items, entries with more than three nonzeros
-                                           (2, 384, 768, 4700, 1, 0.857)])
+                                           (2, 384, 768, 4700, 1, 0.857),
+                                           # entries with five nonzeros (canonical words) on both kernels
+                                           (6, 256, 512, 300, 1, 0.75)])
 def test_moe_layer_parity(dev, E, d, f, T, k, p0):
     dd = Q.Dictionary(dictionary(p0))
     mwi, mwo, Wi, Wo = _layer(E, d, f, p0, seed=21)

@@ -94,23 +94,33 @@ def test_pack_capacity_error(words886):
     assert ei.value.status == Q.QMOE_ECAPACITY
 
 
-@pytest.mark.parametrize("p0", [0.886, 0.857])
+@pytest.mark.parametrize("p0", [0.886, 0.857, 0.75])
 def test_compact_table_lists_every_nonzero(p0):
+    # up to three nonzeros: three 6-bit slots; four nonzeros within the first eight positions: four
+    # 4-bit slots (flag 0x40); anything else (p0 0.75 has five-nonzero entries): the canonical words
     ents = D.generate(p0)
     words = D.pack(ents)
     comp = Q.qmoe_dict_compact(words)
     plane_a = comp[:2 * 65536].view(np.uint16)
     plane_b = comp[2 * 65536:]
+    kinds = set()
     for e, seq in enumerate(ents):
         a, b = int(plane_a[e]), int(plane_b[e])
         assert (a & 15) == len(seq) // 2
         nz = [2 * i + (1 if s == 1 else 0) for i, s in enumerate(seq) if s]
-        if len(nz) > 3:
-            assert b & 64
-        else:
+        if len(nz) <= 3:
             slots = [(a >> 4) & 63, (a >> 10) & 63, b & 63]
             assert slots == nz + [63] * (3 - len(nz))
-            assert not (b & 64)
+            assert b & 0xC0 == 0
+            kinds.add(3)
+        elif len(nz) == 4 and nz[3] < 16:
+            assert [(a >> 4) & 15, (a >> 8) & 15, (a >> 12) & 15, b & 15] == nz
+            assert b & 0xF0 == 0x40
+            kinds.add(4)
+        else:
+            assert a >> 4 == 0xFFF and b == 0xBF
+            kinds.add(5)
+    assert kinds == {0.886: {3}, 0.857: {3, 4}, 0.75: {3, 4, 5}}[p0]
 
 
 def test_rvq_pack_matches_oracle():
