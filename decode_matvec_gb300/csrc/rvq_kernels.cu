@@ -198,10 +198,41 @@ __device__ void fwht_smem_batch(float* s, int n, int count, float norm) {
     __syncthreads();
 }
 
+// Staging scale of one rotated activation row for the tensor-core kernel, which
+// splits each value into an fp16 high part and the fp16 of the remainder: the
+// power of two 2^k that brings the row's largest magnitude into [2^14, 2^15).
+// Both parts then stay inside fp16's range (|v| < 65504 after scaling), and a
+// value loses low bits only when it is below 2^-25 of the row's largest one.
+// Multiplying by 2^k is exact in fp32, so the kernel's output, divided by 2^k
+// again, is what an unbounded split would give.  An all-zero (or non-finite)
+// row keeps 1.  k is kept inside [-126, 126], where 2^k and 2^-k are normal.
+__device__ __forceinline__ float stage_scale_of_max(float mx) {
+    if (!(mx > 0.0f) || !(mx <= 3.402823466e38f)) return 1.0f;
+    int ex;
+    frexpf(mx, &ex);                                   // mx = f * 2^ex, f in [0.5, 1)
+    const int k = max(-126, min(126, 15 - ex));
+    return __int_as_float((127 + k) << 23);
+}
+
+// Largest |v| over a block's values (every thread passes its own maximum); red: 32 floats.
+__device__ __forceinline__ float block_max_abs(float v, float* red) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(QMOE_FULL_MASK, v, d));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();                                   // red may still be read by an earlier call
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
 // x'[row] = H (D_in x[src]) for one or two sign vectors (gate and up share the input).
 __global__ void in_transform_kernel(const uint16_t* __restrict__ x, int x_div, const int32_t* __restrict__ expert_of,
                                     int k_of, const int8_t* __restrict__ si0, const int8_t* __restrict__ si1, int n,
-                                    float norm, float* __restrict__ out0, float* __restrict__ out1) {
+                                    float norm, float* __restrict__ out0, float* __restrict__ out1,
+                                    float* __restrict__ sc0, float* __restrict__ sc1) {
+    __shared__ float red[32];
     extern __shared__ float sm[];
     const int row = blockIdx.x;
     const int e = expert_of ? expert_of[row] : 0;
@@ -216,9 +247,22 @@ __global__ void in_transform_kernel(const uint16_t* __restrict__ x, int x_div, c
     }
     __syncthreads();
     fwht_smem_batch(s0, n, si1 ? 2 : 1, norm);
+    float m0 = 0.0f, m1 = 0.0f;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
         out0[(size_t)row * n + i] = s0[i];
-        if (si1) out1[(size_t)row * n + i] = s1[i];
+        m0 = fmaxf(m0, fabsf(s0[i]));
+        if (si1) {
+            out1[(size_t)row * n + i] = s1[i];
+            m1 = fmaxf(m1, fabsf(s1[i]));
+        }
+    }
+    if (sc0) {
+        const float a0 = block_max_abs(m0, red);
+        if (threadIdx.x == 0) sc0[row] = stage_scale_of_max(a0);
+        if (sc1 && si1) {
+            const float a1 = block_max_abs(m1, red);
+            if (threadIdx.x == 0) sc1[row] = stage_scale_of_max(a1);
+        }
     }
     (void)k_of;
 }
@@ -228,7 +272,8 @@ __global__ void in_transform_kernel(const uint16_t* __restrict__ x, int x_div, c
 __global__ void swiglu_transform_kernel(const float* __restrict__ gp, const float* __restrict__ up,
                                         const int32_t* __restrict__ expert_of, const int8_t* __restrict__ so_g,
                                         const int8_t* __restrict__ so_u, const int8_t* __restrict__ si_d, int n,
-                                        float norm, float* __restrict__ out) {
+                                        float norm, float* __restrict__ out, float* __restrict__ sc) {
+    __shared__ float red[32];
     extern __shared__ float sm[];
     const int row = blockIdx.x;
     const int e = expert_of[row];
@@ -250,7 +295,15 @@ __global__ void swiglu_transform_kernel(const float* __restrict__ gp, const floa
     }
     __syncthreads();
     fwht_smem(sg, n, norm);
-    for (int i = threadIdx.x; i < n; i += blockDim.x) out[(size_t)row * n + i] = sg[i];
+    float mx = 0.0f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        out[(size_t)row * n + i] = sg[i];
+        mx = fmaxf(mx, fabsf(sg[i]));
+    }
+    if (sc) {
+        const float a = block_max_abs(mx, red);
+        if (threadIdx.x == 0) sc[row] = stage_scale_of_max(a);
+    }
 }
 
 // y[t] = sum_j gate[t][j] * D_out H y'[t*k + j]  (k == 1 and gates == NULL: plain output transform).
@@ -323,6 +376,7 @@ __global__ void out_transform_cluster_kernel(const float* __restrict__ yp, const
 struct RvqGemmArgs {
     RvqDev m;
     const float* xr;      // rotated activations, fp32 [slot][cols]
+    const float* xs;      // per-slot power-of-two staging scale of xr for the tensor-core kernel
     const Job* jobs;
     const int* n_jobs_dev;
     const int* slots;
@@ -720,6 +774,9 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
         const int bn = (tid & 7) | ((tid >> 6) << 3), bg = (tid >> 3) & 7;
         const int bslot = bn < job.n_tok ? (a.slots ? a.slots[job.slot_begin + bn] : job.slot_begin + bn) : -1;
         const float* bp = a.xr + (size_t)(bslot < 0 ? 0 : bslot) * m.cols + bg * 16;
+        // the token's staging scale: a power of two, applied before the fp16 split and undone in
+        // the epilogue (exact)
+        const float bscale = bslot >= 0 && a.xs ? __ldg(a.xs + bslot) : 1.0f;
         // the global loads of chunk kc + 1 are issued before chunk kc is decoded
         // a thread's kTcVpt vectors of a chunk: 8 * S code bytes, as S 8-byte loads
         uint2 cw_n[QMOE_RVQ_MAX_STAGES];
@@ -778,8 +835,10 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int c8 = bg * 2 + h2;
-                        const float v[8] = {xv[2 * h2].x, xv[2 * h2].y, xv[2 * h2].z, xv[2 * h2].w,
-                                            xv[2 * h2 + 1].x, xv[2 * h2 + 1].y, xv[2 * h2 + 1].z, xv[2 * h2 + 1].w};
+                        const float v[8] = {xv[2 * h2].x * bscale,     xv[2 * h2].y * bscale,
+                                            xv[2 * h2].z * bscale,     xv[2 * h2].w * bscale,
+                                            xv[2 * h2 + 1].x * bscale, xv[2 * h2 + 1].y * bscale,
+                                            xv[2 * h2 + 1].z * bscale, xv[2 * h2 + 1].w * bscale};
                         const int o = (bn >> 3) * kTcSBO + c8 * kTcLBO + (bn & 7) * 16;
                         store_hi_lo8(Bh + o, Bl + o, v);
                     }
@@ -836,7 +895,9 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
                 for (int n = 0; n < kTcN; ++n) {
                     if (n < job.n_tok) {
                         const int slot = a.slots ? a.slots[job.slot_begin + n] : job.slot_begin + n;
-                        a.out[(size_t)slot * m.rows + row] = s * (__uint_as_float(r[n]) + __uint_as_float(rl2[n]));
+                        const float inv = a.xs ? 1.0f / __ldg(a.xs + slot) : 1.0f;     // exact: a power of two
+                        a.out[(size_t)slot * m.rows + row] =
+                            s * ((__uint_as_float(r[n]) + __uint_as_float(rl2[n])) * inv);
                     }
                 }
             }
@@ -992,7 +1053,8 @@ extern "C" int rvq_decode_dense(const rvq_matrix_set* mat, float* w_out, void* s
 extern "C" int rvq_expert_matmul_ws_size(int rows, int cols, int T, size_t* bytes) {
     qmoe::clear_error();
     if (!bytes || !pow2(rows) || !pow2(cols) || T < 0) return fail(QMOE_EINVAL, "rvq_expert_matmul_ws_size: bad sizes");
-    *bytes = align256(sizeof(float) * (size_t)T * cols) + align256(sizeof(float) * (size_t)T * rows);
+    *bytes = align256(sizeof(float) * (size_t)T * cols) + align256(sizeof(float) * (size_t)T * rows) +
+             align256(sizeof(float) * (size_t)T);
     return QMOE_OK;
 }
 
@@ -1009,14 +1071,17 @@ extern "C" int rvq_expert_matmul(const rvq_matrix_set* mat, const void* x_bf16, 
     cudaStream_t st = (cudaStream_t)stream;
     float* xr = (float*)workspace;
     float* yr = (float*)((char*)workspace + align256(sizeof(float) * (size_t)T * mat->cols));
+    float* xs = (float*)((char*)yr + align256(sizeof(float) * (size_t)T * mat->rows));
     const int rows = mat->rows, cols = mat->cols;
     in_transform_kernel<<<T, fwht_threads(cols), 2 * cols * sizeof(float), st>>>(
-        (const uint16_t*)x_bf16, 1, nullptr, 1, mat->sign_in, nullptr, cols, inv_sqrt(cols), xr, nullptr);
+        (const uint16_t*)x_bf16, 1, nullptr, 1, mat->sign_in, nullptr, cols, inv_sqrt(cols), xr, nullptr, xs,
+        nullptr);
     int rc = qmoe::launch_check("in_transform_kernel");
     if (rc) return rc;
     RvqGemmArgs a{};
     a.m = to_dev(mat);
     a.xr = xr;
+    a.xs = xs;
     a.jobs = nullptr;
     a.slots = nullptr;
     a.T_implicit = T;
@@ -1043,6 +1108,9 @@ struct RvqMoeWs {
     float* up;
     float* hr;
     float* dp;
+    float* xg_s;      // per-slot staging scales of xg, xu and hr (tensor-core kernel)
+    float* xu_s;
+    float* hr_s;
     size_t bytes;
 };
 
@@ -1068,6 +1136,9 @@ RvqMoeWs rvq_moe_layout(void* base, int E, int d_model, int d_ff, int T, int k) 
     w.up = (float*)take(sizeof(float) * slots * d_ff);
     w.hr = (float*)take(sizeof(float) * slots * d_ff);
     w.dp = (float*)take(sizeof(float) * slots * d_model);
+    w.xg_s = (float*)take(sizeof(float) * std::max<size_t>(slots, 1));
+    w.xu_s = (float*)take(sizeof(float) * std::max<size_t>(slots, 1));
+    w.hr_s = (float*)take(sizeof(float) * std::max<size_t>(slots, 1));
     w.bytes = off;
     return w;
 }
@@ -1110,7 +1181,8 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     if (rc) return rc;
     // ids is [T][k] = expert of each flat slot
     in_transform_kernel<<<slots, fwht_threads(d_model), 2 * d_model * sizeof(float), st>>>(
-        (const uint16_t*)x_bf16, k, ids, k, gate->sign_in, up->sign_in, d_model, inv_sqrt(d_model), w.xg, w.xu);
+        (const uint16_t*)x_bf16, k, ids, k, gate->sign_in, up->sign_in, d_model, inv_sqrt(d_model), w.xg, w.xu,
+        w.xg_s, w.xu_s);
     if ((rc = qmoe::launch_check("in_transform_kernel"))) return rc;
     qmoe::phase_event(1, st);
     RvqGemmArgs a{};
@@ -1120,15 +1192,17 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     a.nt_max = nt_a;
     a.m = to_dev(gate);
     a.xr = w.xg;
+    a.xs = w.xg_s;
     a.out = w.gp;
     if ((rc = gemm(a, d_ff))) return rc;
     a.m = to_dev(up);
     a.xr = w.xu;
+    a.xs = w.xu_s;
     a.out = w.up;
     if ((rc = gemm(a, d_ff))) return rc;
     qmoe::phase_event(2, st);
     swiglu_transform_kernel<<<slots, fwht_threads(d_ff), 2 * d_ff * sizeof(float), st>>>(
-        w.gp, w.up, ids, gate->sign_out, up->sign_out, down->sign_in, d_ff, inv_sqrt(d_ff), w.hr);
+        w.gp, w.up, ids, gate->sign_out, up->sign_out, down->sign_in, d_ff, inv_sqrt(d_ff), w.hr, w.hr_s);
     if ((rc = qmoe::launch_check("swiglu_transform_kernel"))) return rc;
     qmoe::phase_event(3, st);
     a.jobs = w.jobs_b;
@@ -1136,6 +1210,7 @@ extern "C" int rvq_moe_layer(const rvq_matrix_set* gate, const rvq_matrix_set* u
     a.nt_max = nt_b;
     a.m = to_dev(down);
     a.xr = w.hr;
+    a.xs = w.hr_s;
     a.out = w.dp;
     if ((rc = gemm(a, d_model))) return rc;
     qmoe::phase_event(4, st);

@@ -207,3 +207,64 @@ def test_rvq_bad_stage_count_reported(dev):
     w = torch.empty((rows, cols), dtype=torch.float32, device=dev)
     Q.rvq_decode_dense(s, w)
     assert Q.qmoe_check_status() == Q.QMOE_EFORMAT
+
+
+# ------------------------------------------------------ activation range of the tensor-core split
+def _scaled_tokens(seed, T, cols, exps):
+    """bf16 tokens N(0,1) * 10**exps[t] (token t's magnitude set by its own exponent)."""
+    v = np.random.default_rng(seed).standard_normal((T, cols)) * (10.0 ** np.asarray(exps, np.float64))[:, None]
+    return synth.bf16_bits_from_f32(v.astype(np.float32))
+
+
+@pytest.mark.parametrize("T", [1, 3, 16, 32])
+def test_rvq_expert_matmul_activation_range(dev, T):
+    """Tokens of very different magnitudes in one batch (|x| up to ~1e6 and down to ~1e-4): the
+    CUDA-core path (T < 16) takes fp32 activations as they are; the tensor-core path (T >= 16)
+    splits each token into fp16 high and low parts after a per-token power-of-two scale, so no
+    part leaves fp16's range.  Every token is compared with the oracle on its own."""
+    rows, cols = 256, 512
+    mt = _matrix(3, 1, 0, rows, cols)
+    s = _set([mt], rows, cols)
+    exps = np.resize(np.array([6.0, -4.0, 0.0, 5.0, -3.0, 2.5, 4.7]), T)
+    xb = _scaled_tokens(8, T, cols, exps)
+    y = torch.empty((T, rows), dtype=torch.float32, device=dev)
+    ws = torch.empty(Q.rvq_expert_matmul_ws_size(rows, cols, T), dtype=torch.uint8, device=dev)
+    Q.rvq_expert_matmul(s, bf16_tensor(xb), y, ws)
+    assert Q.qmoe_check_status() == Q.QMOE_OK
+    ref = R.linear(synth.bf16_to_f64(xb), R.decode(mt["idx"], mt["cb"], mt["scale"]), mt["so"], mt["si"])
+    got = y.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    for t in range(T):
+        assert P.normwise_rel_err(got[t], ref[t]) < TOL, (t, exps[t])
+
+
+def test_rvq_moe_layer_activation_range(dev):
+    """The SwiGLU layer on the tensor-core path with tokens scaled by 1e5 and 1e-3: gate/up inputs,
+    the bf16 h (up to ~1e9 here) and the down input all pass through the fp16 split."""
+    E, d, f, T, k, seed = 8, 256, 128, 32, 4, 33
+    gate = [_matrix(seed, e, synth.GATE, f, d) for e in range(E)]
+    cb = R.f16_round(gate[0]["cb"].view(np.float16).astype(np.float64))
+    gate = [_matrix(seed, e, synth.GATE, f, d, cb=cb) for e in range(E)]
+    up = [_matrix(seed, e, synth.UP, f, d, cb=cb) for e in range(E)]
+    down = [_matrix(seed, e, synth.DOWN, d, f, cb=cb) for e in range(E)]
+    sg, su, sd = _set(gate, f, d), _set(up, f, d), _set(down, d, f)
+    lg = synth.zipf_logits(seed, T, E, 0.9)
+    xb = _scaled_tokens(9, T, d, np.where(np.arange(T) % 2 == 0, 5.0, -3.0))
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+    Q.qmoe_route(torch.from_numpy(lg).to(dev), k, ids, gates)
+    ws = torch.empty(Q.rvq_moe_layer_ws_size(E, d, f, T, k), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    Q.rvq_moe_layer(sg, su, sd, bf16_tensor(xb), ids, gates, y, ws)
+    assert Q.qmoe_check_status() == Q.QMOE_OK
+    rid, rg = M.route(lg, k)
+
+    def expert(e, xs):
+        trip = [(R.decode(m["idx"], m["cb"], m["scale"]), m["so"], m["si"]) for m in (gate[e], up[e], down[e])]
+        return R.swiglu_expert(xs, *trip)
+
+    ref = M.moe_layer(synth.bf16_to_f64(xb), rid, rg, expert, d)
+    got = y.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    for t in range(T):
+        assert P.normwise_rel_err(got[t], ref[t]) < TOL, t
