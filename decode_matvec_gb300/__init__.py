@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "QMOE_OK", -1: "QMOE_EINVAL", -2: "QMOE_ECAPACITY", -3: "QMOE
                 -5: "QMOE_ETIMEOUT", -6: "QMOE_EUNSUPPORTED"}
 DICT_ENTRIES = 65536
 DICT_WORDS = 2 * DICT_ENTRIES
-COMPACT_BYTES = 3 * DICT_ENTRIES
+COMPACT_BYTES = 7 * DICT_ENTRIES
 QMOE_VQ_RVQ, QMOE_VQ_E8P = 0, 1      # code formats of an RVQ matrix set
 
 EXPORTED = [

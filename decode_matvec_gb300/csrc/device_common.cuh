@@ -17,6 +17,17 @@ namespace qmoe {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The limit is a per-kernel, per-device setting, so the call
+// reaches the runtime once per (kernel, device, larger size); later launches
+// only look it up.
+int smem_attr(const void* kernel, int bytes, const char* where);
+
+// The calling thread's current CUDA context (the driver's handle), or NULL
+// when it cannot be read.  Per-device caches key on it as well, so that a
+// device reset or a caller-created context never reuses a stale entry.
+void* current_context();
+
 // Records a CUDA failure (if any) and returns QMOE_ECUDA, else QMOE_OK.
 inline int cuda_check(cudaError_t e, const char* where) {
     if (e == cudaSuccess) return QMOE_OK;

@@ -34,7 +34,8 @@ __device__ int g_dict_error;
 __device__ __forceinline__ void set_error(int code) { atomicCAS(&g_dict_error, 0, code); }
 
 constexpr int kDictA = 2 * QMOE_DICT_ENTRIES;          // bytes of the uint16 plane
-constexpr int kDictBytes = QMOE_COMPACT_BYTES;          // both planes
+constexpr int kDictBytes = 3 * QMOE_DICT_ENTRIES;       // the uint16 and uint8 planes (staged in SMEM)
+constexpr int kDictWordsOff = 3 * QMOE_DICT_ENTRIES;    // byte offset of the uint32 plane
 constexpr int kSlotEmpty = 63;
 constexpr int kSmemMax = 232448;                        // 227 KB opt-in per block
 constexpr int kBudgetSmemDict = kSmemMax - kDictBytes - 256;   // activations + row sums, dictionary in SMEM
@@ -96,6 +97,7 @@ struct GemmArgs {
     const uint16_t* dictA;       // compact plane A (uint16 per entry)
     const uint8_t* dictB;        // compact plane B (uint8 per entry)
     const uint32_t* words;       // canonical entries (for escape entries)
+    const uint32_t* dictW;       // compact entries as one uint32 each (reads from global memory)
     MatDev m;
     const uint16_t* x;           // bf16 rows of `cols` values
     int x_div;                   // source row of slot s is s / x_div
@@ -636,69 +638,115 @@ __global__ void __launch_bounds__(GemmBounds<DICT_SMEM, NTMAX>::threads, GemmBou
 // ------------------------------------------------------------ tensor-core path for experts with many tokens
 // An expert that receives many tokens is a real dense contraction, and the
 // QMoE page's own suggestion for large token counts is to decompress first and
-// then multiply.  Here the decompression goes to shared memory only: for each
-// 256-weight block of 128 rows, 128 threads expand the rows' codewords into a
-// dense bf16 tile of exact {-1, 0, +1} (one thread per row, nonzeros only,
-// over a zero-filled tile) while the other 128 threads stage the block's
-// activations of up to 64 tokens as bf16; one thread then issues
-// tcgen05.mma (M=128, N=64, K=16, bf16 x bf16 -> fp32 in tensor memory).
-// The row scale is applied in the epilogue, so the product is the same
-// s * sum(+-x) as the CUDA-core kernel, summed in another order.  Each block
-// of ~97 KB of shared memory holds one stage; two blocks per SM overlap one
-// block's decoding with the other's MMAs.  Waits are bounded (QMOE_ETIMEOUT).
+// then multiply.  Here the decompression goes to shared memory only, in a
+// warp-specialised pipeline (one persistent CTA per SM):
+//  * 8 decoder warps, in two groups of 128 threads, expand the codewords of a
+//    256-column block of 128 rows into a dense bf16 tile of exact {-1, 0, +1}
+//    (one thread per row: its row is zeroed, then its nonzeros written); the
+//    groups take alternate blocks, so two blocks are decoded at once;
+//  * a loader warp stages the block's activations of up to 64 tokens (bf16,
+//    16-byte asynchronous copies, zero past the tokens and columns that exist);
+//  * one thread issues tcgen05.mma (M=128, N = tokens rounded up to 16, K=16,
+//    bf16 x bf16 -> fp32 in tensor memory) and commits each block to the
+//    barrier that frees its two stages;
+//  * 4 epilogue warps read a finished tile's accumulators (two accumulators in
+//    tensor memory alternate between tiles), apply the row scale and the
+//    activation or gate, and store.
+// Tiles are 128-byte-swizzled K-major (64-column atoms of 8-row groups
+// 1024 bytes apart), the layout the tensor core reads at full rate.  The row
+// scale is applied in the epilogue, so the product is the same s * sum(+-x)
+// as the CUDA-core kernel, summed in another order.  Every wait is bounded:
+// on expiry the kernel records QMOE_ETIMEOUT, waits (bounded) for its
+// outstanding MMAs, frees its tensor memory and returns.
 constexpr int kDtcM = 128, kDtcN = 64, kDtcK = 256;
-constexpr int kDtcThreads = 256;
-constexpr uint32_t kDtcLBO = 128, kDtcSBO = (kDtcK / 8) * 128;      // 4096 B
-constexpr int kDtcABytes = kDtcM * kDtcK * 2;                        // 64 KB
-constexpr int kDtcBBytes = kDtcN * kDtcK * 2;                        // 32 KB
-constexpr int kDtcSmem = 1024 + kDtcABytes + kDtcBBytes + 64 + 4 * kDtcN;
-constexpr uint32_t kDtcIdesc = qmoe_tc::idesc_f16(kDtcM, kDtcN, true, true);
-constexpr uint32_t kDtcSpin = 1u << 20;
+constexpr int kDtcStageA = kDtcM * kDtcK * 2;                 // 64 KB per A stage
+constexpr int kDtcStageB = kDtcN * kDtcK * 2;                 // 32 KB per B stage
+constexpr int kDtcAtomA = kDtcM * 128;                        // one 64-column atom of A (16 KB)
+constexpr int kDtcAtomB = kDtcN * 128;                        // ... of B (8 KB)
+constexpr int kDtcDecWarps = 8, kDtcEpiWarp = 8, kDtcLoadWarp = 12, kDtcMmaWarp = 13;
+constexpr int kDtcThreads = 14 * 32;
+constexpr int kDtcTmemCols = 2 * kDtcN;                       // two accumulators
+constexpr int kDtcStagesB = 3;                                 // activation stages (the loader runs ahead)
+constexpr int kDtcSmem = 1024 + 2 * kDtcStageA + kDtcStagesB * kDtcStageB + 192;
+constexpr uint32_t kDtcSpin = 1u << 22;
 constexpr uint16_t kBf16One = 0x3F80, kBf16MinusOne = 0xBF80;
 
-__device__ __forceinline__ void store_out(const GemmArgs& a, int slot, int row, float v) {
-    const size_t o = (size_t)slot * a.m.rows + row;
-    switch (a.mode) {
-        case OUT_PLAIN:
-            if (a.y_is_f32) ((float*)a.out)[o] = v;
-            else ((uint16_t*)a.out)[o] = f32_to_bf16(v);
-            break;
-        case OUT_RELU_H:
-            ((uint16_t*)a.out)[o] = f32_to_bf16(fmaxf(v, 0.0f));
-            break;
-        case OUT_GATED: {
-            const float g = a.gates[slot] * v;
-            if (a.y_is_f32) ((float*)a.out)[o] = g;
-            else ((uint16_t*)a.out)[o] = f32_to_bf16(g);
-            break;
-        }
-        default:
-            ((float*)a.out)[o] = v;
-            break;
-    }
+// Byte offset of element (r, c) in a 128-byte-swizzled K-major bf16 tile whose
+// 64-column atoms are atom_bytes apart: 16-byte chunk (c / 8) % 8 of row r sits at
+// chunk position ((c / 8) % 8) ^ (r % 8) of its 128-byte line.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom_bytes) {
+    return (uint32_t)(c >> 6) * atom_bytes + (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u +
+           ((uint32_t)(((c >> 3) & 7) ^ (r & 7)) << 4) + (uint32_t)(c & 7) * 2u;
+}
+
+// Descriptor of a 128-byte-swizzled K-major operand (tcgen05 version 1, 8-row groups 1024 B apart).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;                   // leading byte offset: unused for swizzled K-major
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;                                    // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(qmoe_tc::smem_u32(bar)) : "memory");
 }
 
 // Component q (0..3, a constant after unrolling) of a uint4.
 __device__ __forceinline__ uint32_t u4_at(const uint4& v, int q) { return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w; }
 
-// One thread expands the codewords [lo, hi) (absolute indices into `codes`)
-// of (row, block) into its row of the tile.  Codewords are read 16 at a time
-// as aligned 16-byte chunks, then all their compact entries, so that a block
-// costs a few memory round trips instead of two per codeword.
-// The block's codeword range and its first 16-codeword window, loaded one block ahead (while the
-// previous block's MMAs run).  `ok` is false for a range no valid block can have (every codeword
-// covers at least two weights); then nothing is loaded.
-struct RowBlockAhead {
+// Bounded wait for the phase of the given parity; a thread whose phase has not
+// completed is suspended (up to about a microsecond per try) instead of
+// spinning, so waiting warps leave the issue slots to the working ones.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    const uint32_t b = qmoe_tc::smem_u32(bar);
+    for (uint32_t it = 0; it < limit; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(b), "r"(parity), "r"(1000u)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// 8 consecutive fp32 accumulator columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+
+// Weights of an entry outside the compact slots, from its canonical words (rare: five or more
+// nonzeros, or a fourth one past the eighth position).
+__device__ __forceinline__ void canonical_to_row(const uint32_t* words, uint32_t code, int len, int col, unsigned char* A,
+                                              int rl) {
+    const uint32_t c0 = __ldg(words + 2 * code), c1 = __ldg(words + 2 * code + 1);
+    for (int q = 0; q < len; ++q) {
+        const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
+        if (s) *(uint16_t*)(A + sw128_off(rl, col + q, kDtcAtomA)) = s == 1u ? kBf16MinusOne : kBf16One;
+    }
+}
+
+// The codeword range of one (row, 256-column block) and its first two aligned
+// 16-byte chunks of codewords, loaded one block ahead of its decoding.  `ok` is
+// false for a range no valid block can have (every codeword covers at least two
+// weights); nothing is loaded then.
+struct RowBlk {
     uint64_t lo, hi;
     uint4 ch0, ch1;
     bool ok;
 };
 
-__device__ __forceinline__ RowBlockAhead load_row_block(const uint16_t* codes, const uint32_t* off, uint64_t cbase,
-                                                        int row, int nb, int b, int blen) {
-    RowBlockAhead p;
-    p.lo = cbase + off[(size_t)row * nb + b];
-    p.hi = cbase + off[(size_t)row * nb + b + 1];
+__device__ __forceinline__ RowBlk load_rowblk(const uint16_t* codes, uint2 range, uint64_t cbase, int blen) {
+    RowBlk p;
+    p.lo = cbase + range.x;
+    p.hi = cbase + range.y;
     p.ok = !(p.hi < p.lo || p.hi - p.lo > (uint64_t)(blen / 2));
     const uint64_t c8 = p.lo & ~7ull;
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -707,181 +755,339 @@ __device__ __forceinline__ RowBlockAhead load_row_block(const uint16_t* codes, c
     return p;
 }
 
-__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, const RowBlockAhead& p,
-                                                 int blen, unsigned char* A, int rl, bool& bad) {
-    unsigned char* rowbase = A + (rl >> 3) * kDtcSBO + (rl & 7) * 16;
-    const uint64_t lo = p.lo, hi = p.hi;
+// Start and end codeword of block b of a row (relative to the expert's base).
+__device__ __forceinline__ uint2 load_range(const uint32_t* off_row, int b) {
+    return make_uint2(__ldg(off_row + b), __ldg(off_row + b + 1));
+}
+
+// One thread expands the codewords of one (row, block) into the tile row `rl`
+// (bf16 +-1 at the nonzeros of an already zeroed row).  The codewords come 16 at
+// a time as two aligned 16-byte chunks (the first two preloaded); the 16 compact
+// entries are gathered with unconditional loads (out-of-range positions read
+// entry 0 and are ignored) so that they are all in flight at once: a block costs
+// about one memory round trip.  `bad` is set for a block that does not expand
+// to exactly blen weights.
+__device__ __forceinline__ void decode_row_block(const GemmArgs& a, const uint16_t* codes, const RowBlk& p, int blen,
+                                                 unsigned char* A, int rl, bool& bad) {
     if (!p.ok) {
         bad = true;
         return;
     }
+    const uint32_t arow = qmoe_tc::smem_u32(A) + (uint32_t)(rl >> 3) * 1024u + (uint32_t)(rl & 7) * 128u;
+    const uint32_t rsw = (uint32_t)(rl & 7) << 4;
     int col = 0;
-    for (uint64_t c8 = lo & ~7ull; c8 < hi; c8 += 16) {
-        const bool first = c8 == (lo & ~7ull);
+    for (uint64_t c8 = p.lo & ~7ull; c8 < p.hi; c8 += 16) {
+        const bool first = c8 == (p.lo & ~7ull);
         const uint4 ch0 = first ? p.ch0 : __ldg((const uint4*)(codes + c8));
-        const uint4 ch1 = first ? p.ch1 : c8 + 8 < hi ? __ldg((const uint4*)(codes + c8 + 8)) : make_uint4(0, 0, 0, 0);
-        uint32_t code[16], ea[16], eb[16];
+        const uint4 ch1 = first ? p.ch1 : c8 + 8 < p.hi ? __ldg((const uint4*)(codes + c8 + 8)) : make_uint4(0, 0, 0, 0);
+        uint32_t code[16], e[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
             const uint32_t w = u4_at(k < 8 ? ch0 : ch1, (k >> 1) & 3);
             code[k] = (w >> (16 * (k & 1))) & 0xFFFFu;
-            const bool in = c8 + k >= lo && c8 + k < hi;
-            ea[k] = in ? (uint32_t)__ldg(a.dictA + code[k]) : 0u;
-            eb[k] = in ? (uint32_t)__ldg(a.dictB + code[k]) : 63u;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) e[k] = __ldg(a.dictW + code[k]);
+        // run starts of the 16 positions (out-of-range positions have length 0), then every store of
+        // the batch independently of the others
+        int start[16];
+        uint32_t esc = 0;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const bool in = c8 + k >= p.lo && c8 + k < p.hi;
+            if (!in) e[k] = 0x3F0000u | 0xFFF0u;          // length 0, empty slots
+            start[k] = col;
+            col += (int)(e[k] & 15u) * 2;
+            esc |= e[k];
+        }
+        if (col > blen) {
+            bad = true;
+            return;
         }
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-            const int len = (int)(ea[k] & 15u) * 2;
-            if (len == 0) continue;                       // outside [lo, hi): every entry has a pair
-            if (col + len > blen) {
-                bad = true;
-                break;
-            }
-            if (eb[k] & 0x80u) {
-                const uint32_t c0 = __ldg(a.words + 2 * code[k]), c1 = __ldg(a.words + 2 * code[k] + 1);
-                for (int q = 0; q < len; ++q) {
-                    const uint32_t s = ((q < 14 ? c0 : c1) >> (4 + 2 * (q % 14))) & 3u;
-                    if (s) {
-                        const int c = col + q;
-                        *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) = s == 1u ? kBf16MinusOne : kBf16One;
-                    }
-                }
-            } else {
-                uint32_t sl[4];
-                entry_slots<true>(ea[k], eb[k], sl);
+            const uint32_t ea = e[k] & 0xFFFFu, eb = e[k] >> 16;
+            // the entry's slots as four 6-bit fields (63 = empty)
+            const uint32_t w = (eb & 0x40u) ? (((ea >> 4) & 15u) | (((ea >> 8) & 15u) << 6) | ((ea >> 12) << 12) |
+                                               ((eb & 15u) << 18))
+                                            : ((ea >> 4) | ((eb & 63u) << 12) | (63u << 18));
 #pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    if (sl[z] != 63u) {
-                        const int c = col + (int)(sl[z] >> 1);
-                        *(uint16_t*)(rowbase + (c >> 3) * kDtcLBO + (c & 7) * 2) =
-                            (sl[z] & 1u) ? kBf16MinusOne : kBf16One;
-                    }
+            for (int z = 0; z < 4; ++z) {
+                const uint32_t sl = (w >> (6 * z)) & 63u;
+                if (z == 3 && !(esc & 0x400000u)) break;      // no entry of the batch has a fourth slot
+                if (sl != 63u) {
+                    const uint32_t c = (uint32_t)start[k] + (sl >> 1);
+                    const uint32_t sa = arow + (c >> 6) * (uint32_t)kDtcAtomA + (((c << 1) & 127u) ^ rsw);
+                    const uint16_t v = (uint16_t)(kBf16One | ((sl & 1u) << 15));
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa), "h"(v) : "memory");
                 }
             }
-            col += len;
         }
-        if (bad) break;
+        if (esc & 0x800000u) {
+            // entries outside the compact slots: from their canonical words (rare)
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if ((e[k] >> 16) & 0x80u) canonical_to_row(a.words, code[k], (int)(e[k] & 15u) * 2, start[k], A, rl);
+        }
     }
     if (col != blen) bad = true;
 }
 
-__global__ void __launch_bounds__(kDtcThreads, 2) dict_tc_kernel(const GemmArgs a) {
+
+// Scale, activation or gate, and store of one token column of a finished tile.
+template <int MODE>
+__device__ __forceinline__ void tc_store(const GemmArgs& a, int slot, int row, float v) {
+    const size_t o = (size_t)slot * a.m.rows + row;
+    if constexpr (MODE == OUT_RELU_H) {
+        ((uint16_t*)a.out)[o] = f32_to_bf16(fmaxf(v, 0.0f));
+    } else if constexpr (MODE == OUT_SLOT_F32) {
+        ((float*)a.out)[o] = v;
+    } else {
+        const float g = MODE == OUT_GATED ? a.gates[slot] * v : v;
+        if (a.y_is_f32) ((float*)a.out)[o] = g;
+        else ((uint16_t*)a.out)[o] = f32_to_bf16(g);
+    }
+}
+
+// A finished tile's outputs: lane i of the warp holds the slots of tokens i and i + 32 and hands
+// each to the whole warp when its column is stored.
+template <int MODE>
+__device__ __forceinline__ void tc_epilogue_tile(const GemmArgs& a, uint32_t taddr, int slot_lo, int slot_hi, int n_tok,
+                                                 int row, float s) {
+    for (int n0 = 0; n0 < n_tok; n0 += 8) {
+        uint32_t r[8];
+        tmem_ld8(taddr + (uint32_t)n0, r);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int n = n0 + q;
+            const int slot = __shfl_sync(QMOE_FULL_MASK, n < 32 ? slot_lo : slot_hi, n & 31);
+            if (n < n_tok && row < a.m.rows) tc_store<MODE>(a, slot, row, s * __uint_as_float(r[q]));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs a) {
     using namespace qmoe_tc;
     unsigned char* smem = (unsigned char*)(((uintptr_t)g_smem + 1023) & ~(uintptr_t)1023);
-    unsigned char* A = smem;
-    unsigned char* B = smem + kDtcABytes;
-    uint64_t* bar = (uint64_t*)(B + kDtcBBytes);
-    uint32_t* tmem_slot = (uint32_t*)(bar + 1);
-    int* sslot = (int*)(tmem_slot + 4);           // the tile's token slots, read once per tile
+    unsigned char* stA = smem;                                   // 2 stages
+    unsigned char* stB = smem + 2 * kDtcStageA;                  // 2 stages
+    uint64_t* bars = (uint64_t*)(stB + kDtcStagesB * kDtcStageB);
+    uint64_t* full_a = bars;          // [2] decoders of a stage's group (4 warp arrivals)
+    uint64_t* empty_a = bars + 2;     // [2] MMA commit: the A stage was read
+    uint64_t* acc_full = bars + 4;    // [2] MMA commit: a tile's accumulator is final
+    uint64_t* acc_empty = bars + 6;   // [2] epilogue warps (4 arrivals): the accumulator was read
+    uint64_t* full_b = bars + 8;      // [3] loader (1 arrival)
+    uint64_t* empty_b = bars + 11;    // [3] MMA commit: the B stage was read
+    uint32_t* tmem_slot = (uint32_t*)(bars + 14);
+    int* abort_flag = (int*)(tmem_slot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const MatDev& m = a.m;
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(full_a + s, 4);
+            mbar_init(empty_a + s, 1);
+            mbar_init(acc_full + s, 1);
+            mbar_init(acc_empty + s, 4);
+        }
+        for (int s = 0; s < kDtcStagesB; ++s) {
+            mbar_init(full_b + s, 1);
+            mbar_init(empty_b + s, 1);
+        }
+        *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kDtcN);
+    if (warp == 0) tmem_alloc(tmem_slot, kDtcTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t phase = 0;
-    bool timed_out = false, bad = false;
+    volatile int* abort_v = abort_flag;
     const int n_jobs = *a.n_jobs_dev;
     const int n_tiles = n_jobs * a.row_tiles;
-    for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
-        const Job job = a.jobs[tile / a.row_tiles];
-        const int r0 = (tile % a.row_tiles) * kDtcM;
-        if (tid < kDtcN) sslot[tid] = tid < job.n_tok ? a.slots[job.slot_begin + tid] : 0;
-        __syncthreads();
-        const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
-        const uint64_t cbase = m.code_base ? m.code_base[job.matrix] : 0ull;
-        const int drow = r0 + tid;                       // the row a decoding thread (tid < kDtcM) expands
-        const bool decodes = tid < kDtcM && drow < m.rows;
-        RowBlockAhead ahead{};
-        if (decodes) ahead = load_row_block(m.codes, off, cbase, drow, m.nb, 0, min(kDtcK, m.cols));
-        for (int b = 0; b < m.nb; ++b) {
-            const int blen = min(kDtcK, m.cols - b * kDtcK);
-            if (tid < kDtcM) {
-                // zero this thread's tile row (16 bytes per store; 8 consecutive rows fill a core
-                // matrix), then write its nonzeros
-                unsigned char* rowbase = A + (tid >> 3) * kDtcSBO + (tid & 7) * 16;
-#pragma unroll 8
-                for (int j = 0; j < kDtcK / 8; ++j) *(uint4*)(rowbase + j * kDtcLBO) = make_uint4(0, 0, 0, 0);
-                if (decodes) decode_row_block(a, m.codes, ahead, blen, A, tid, bad);
-            } else {
-                // activations: 64 tokens x 256 columns in 16-byte asynchronous copies
-                // (zero-filled past the tokens and columns that exist), all in flight at once
-                for (int q = tid - kDtcM; q < kDtcN * (kDtcK / 8); q += kDtcThreads - kDtcM) {
-                    const int n = q / (kDtcK / 8), c8 = q % (kDtcK / 8);
-                    const bool live = n < job.n_tok && c8 * 8 < blen;
-                    const uint16_t* src = a.x;
-                    if (live) src = a.x + (size_t)(sslot[n] / a.x_div) * m.cols + b * kDtcK + c8 * 8;
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                                     smem_u32(B + (n >> 3) * kDtcSBO + c8 * kDtcLBO + (n & 7) * 16)),
-                                 "l"(src), "r"(live ? 16 : 0)
-                                 : "memory");
+    const int nb = m.nb;
+    bool timed_out = false, bad = false;
+
+    if (warp < kDtcDecWarps) {
+        // ---------------- decoders: group g fills stage g for the global blocks g, g + 2, ...
+        const int group = warp >> 2, rl = tid & (kDtcM - 1);
+        uint32_t gb = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+            const Job job = a.jobs[tile / a.row_tiles];
+            const int row = (tile % a.row_tiles) * kDtcM + rl;
+            const bool live = row < m.rows;
+            const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * nb + 1) + (size_t)row * nb;
+            const uint64_t cbase = m.code_base ? m.code_base[job.matrix] : 0ull;
+            // the group's blocks of the tile are b_first, b_first + 2, ...; the memory reads run ahead of
+            // the decoding: a block's codeword range two of the group's blocks ahead, its first codewords
+            // one ahead, so that decoding a block waits only for its dictionary entries
+            const int b_first = (int)((group - (int)(gb & 1u)) & 1);
+            const uint2 z2 = make_uint2(0u, 0u);
+            const uint2 r_first = live && b_first < nb ? load_range(off, b_first) : z2;
+            uint2 r_ahead = live && b_first + 2 < nb ? load_range(off, b_first + 2) : z2;
+            RowBlk cur{};
+            if (live && b_first < nb) cur = load_rowblk(m.codes, r_first, cbase, min(kDtcK, m.cols - b_first * kDtcK));
+            for (int b = 0; b < nb; ++b, ++gb) {
+                if ((int)(gb & 1u) != group) continue;
+                RowBlk nxt{};
+                if (live && b + 2 < nb) nxt = load_rowblk(m.codes, r_ahead, cbase, min(kDtcK, m.cols - (b + 2) * kDtcK));
+                r_ahead = live && b + 4 < nb ? load_range(off, b + 4) : z2;
+                if (!mbar_wait_sleep(empty_a + group, ((gb >> 1) & 1u) ^ 1u, kDtcSpin) || *abort_v) {
+                    timed_out = true;
+                    break;
                 }
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                unsigned char* A = stA + group * kDtcStageA;
+                // zero this thread's row: chunk j of each 128-byte line at swizzled position j ^ (row % 8),
+                // so the 32 rows of a warp write 32 different banks per store
+#pragma unroll 8
+                for (int j = 0; j < kDtcK / 8; ++j) {
+                    const uint32_t pos = (uint32_t)((j ^ rl) & 7);
+                    *(uint4*)(A + (uint32_t)(j >> 3) * kDtcAtomA + (uint32_t)(rl >> 3) * 1024u + (uint32_t)(rl & 7) * 128u +
+                              (pos << 4)) = make_uint4(0, 0, 0, 0);
+                }
+                if (live) decode_row_block(a, m.codes, cur, min(kDtcK, m.cols - b * kDtcK), A, rl, bad);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_a + group);
+                cur = nxt;
             }
-            fence_async_shared();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
-                const int ksteps = (blen + 15) / 16;
-                for (int k = 0; k < ksteps; ++k)
-                    mma_f16(tmem, umma_desc(a0 + k * 2 * kDtcLBO, kDtcLBO, kDtcSBO),
-                            umma_desc(b0 + k * 2 * kDtcLBO, kDtcLBO, kDtcSBO), kDtcIdesc, b > 0 || k > 0);
-                mma_commit(bar);
-            }
-            // the next block's codeword range and first window, while the MMAs run
-            if (decodes && b + 1 < m.nb)
-                ahead = load_row_block(m.codes, off, cbase, drow, m.nb, b + 1, min(kDtcK, m.cols - (b + 1) * kDtcK));
-            // the tiles are rewritten by the next block: wait for these MMAs
-            if (!mbar_wait(bar, phase & 1u, kDtcSpin)) timed_out = true;
-            ++phase;
-            if (__syncthreads_or(timed_out)) {
+        }
+    } else if (warp < kDtcEpiWarp + 4) {
+        // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        const int ew = warp - kDtcEpiWarp;
+        uint32_t t = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x, ++t) {
+            const Job job = a.jobs[tile / a.row_tiles];
+            const int row = (tile % a.row_tiles) * kDtcM + 32 * ew + lane;
+            const uint32_t acc = t & 1u;
+            const int slot_lo = lane < job.n_tok ? a.slots[job.slot_begin + lane] : 0;
+            const int slot_hi = lane + 32 < job.n_tok ? a.slots[job.slot_begin + lane + 32] : 0;
+            const float s = row < m.rows ? f16_to_f32(m.scale[(size_t)job.matrix * m.rows + row]) : 0.0f;
+            if (!mbar_wait_sleep(acc_full + acc, (t >> 1) & 1u, kDtcSpin) || *abort_v) {
                 timed_out = true;
                 break;
             }
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * ew) << 16) + acc * kDtcN;
+            switch (a.mode) {
+                case OUT_RELU_H: tc_epilogue_tile<OUT_RELU_H>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
+                case OUT_GATED: tc_epilogue_tile<OUT_GATED>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
+                case OUT_SLOT_F32: tc_epilogue_tile<OUT_SLOT_F32>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
+                default: tc_epilogue_tile<OUT_PLAIN>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + acc);
         }
-        if (timed_out) break;
-        tc_fence_after();
-        if (warp < 4) {
-            const int row = r0 + 32 * warp + lane;
-            const float s = row < m.rows ? f16_to_f32(m.scale[(size_t)job.matrix * m.rows + row]) : 0.0f;
+    } else if (warp == kDtcLoadWarp) {
+        // ---------------- loader: activations of block b into stage b % 3; a stage is announced once
+        // the copies of the next block are issued (so its own copies have had a block's time to land)
+        uint32_t gb = 0;
+        int pending = -1;                                   // block whose copies are in flight
+        for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+            const Job job = a.jobs[tile / a.row_tiles];
+            const uint16_t* src[2];
+            uint32_t rowo[2], sw[2];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32u * half, r);
-                if (row < m.rows) {
+            for (int i = 0; i < 2; ++i) {
+                const int n = lane + 32 * i;
+                src[i] = n < job.n_tok ? a.x + (size_t)(a.slots[job.slot_begin + n] / a.x_div) * m.cols : a.x;
+                rowo[i] = (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u;
+                sw[i] = (uint32_t)(n & 7);
+            }
+            const bool has[2] = {lane < job.n_tok, lane + 32 < job.n_tok};
+            for (int b = 0; b < nb; ++b, ++gb) {
+                const uint32_t s = gb % kDtcStagesB, use = gb / kDtcStagesB;
+                if (!mbar_wait_sleep(empty_b + s, (use & 1u) ^ 1u, kDtcSpin) || *abort_v) {
+                    timed_out = true;
+                    break;
+                }
+                const uint32_t B = smem_u32(stB + s * kDtcStageB);
+                const int c0 = b * kDtcK;
+                const int live_ch = min(kDtcK, m.cols - c0) / 8;     // whole 16-byte chunks of the block
 #pragma unroll
-                    for (int n = 0; n < 32; ++n) {
-                        const int nn = 32 * half + n;
-                        if (nn < job.n_tok) store_out(a, sslot[nn], row, s * __uint_as_float(r[n]));
+                for (int i = 0; i < 2; ++i) {
+                    const uint16_t* p = src[i] + c0;
+#pragma unroll 8
+                    for (int ch = 0; ch < kDtcK / 8; ++ch) {
+                        const bool live = has[i] && ch < live_ch;
+                        const uint32_t dst = B + (uint32_t)(ch >> 3) * kDtcAtomB + rowo[i] + (((uint32_t)ch ^ sw[i]) & 7u) * 16u;
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                                     "l"(live ? p + ch * 8 : a.x), "r"(live ? 16 : 0)
+                                     : "memory");
                     }
                 }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                if (pending >= 0) {
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                    fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full_b + (uint32_t)pending % kDtcStagesB);
+                }
+                pending = (int)gb;
             }
         }
-        tc_fence_before();
-        __syncthreads();
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (pending >= 0) {
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_b + (uint32_t)pending % kDtcStagesB);
+        }
+    } else if (lane == 0) {
+        // ---------------- MMA issuer
+        uint32_t gb = 0, t = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x, ++t) {
+            const Job job = a.jobs[tile / a.row_tiles];
+            const uint32_t acc = t & 1u;
+            if (!mbar_wait_sleep(acc_empty + acc, ((t >> 1) & 1u) ^ 1u, kDtcSpin) || *abort_v) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            const int n16 = min(kDtcN, (job.n_tok + 15) & ~15);
+            const uint32_t idesc = idesc_f16(kDtcM, n16, true, true);
+            for (int b = 0; b < nb; ++b, ++gb) {
+                const uint32_t s = gb & 1u, sb = gb % kDtcStagesB;
+                if (!mbar_wait_sleep(full_a + s, (gb >> 1) & 1u, kDtcSpin) ||
+                    !mbar_wait_sleep(full_b + sb, (gb / kDtcStagesB) & 1u, kDtcSpin) || *abort_v) {
+                    timed_out = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(stA + s * kDtcStageA), b0 = smem_u32(stB + sb * kDtcStageB);
+                const int ksteps = (min(kDtcK, m.cols - b * kDtcK) + 15) / 16;
+                for (int k = 0; k < ksteps; ++k) {
+                    const uint32_t ko = (uint32_t)(k & 3) * 32u;
+                    mma_f16(tmem + acc * kDtcN, umma_desc_sw128(a0 + (uint32_t)(k >> 2) * kDtcAtomA + ko),
+                            umma_desc_sw128(b0 + (uint32_t)(k >> 2) * kDtcAtomB + ko), idesc, b > 0 || k > 0);
+                }
+                mma_commit(empty_a + s);
+                mma_commit(empty_b + sb);
+            }
+            if (timed_out) break;
+            mma_commit(acc_full + acc);
+        }
+        if (timed_out) {
+            *abort_v = 1;
+            // the tensor core may still be working on committed blocks: wait (bounded) for the last
+            // commit before the memory is released
+            if (gb > 0) mbar_wait_sleep(empty_a + ((gb - 1) & 1u), ((gb - 1) >> 1) & 1u, kDtcSpin);
+        }
     }
+    if (timed_out) *abort_v = 1;
     if (bad) set_error(QMOE_EFORMAT);
-    if (timed_out && tid == 0) set_error(QMOE_ETIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, kDtcN);
+    if (tid == 0 && *abort_v) set_error(QMOE_ETIMEOUT);
+    if (warp == 0) tmem_dealloc(tmem, kDtcTmemCols);
 }
 
 int launch_dict_tc(GemmArgs a, cudaStream_t st, long long tiles_hint) {
-    int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDtcSmem),
-                              "dict tc attr");
+    int rc = qmoe::smem_attr((const void*)dict_tc_kernel, kDtcSmem, "dict tc attr");
     if (rc) return rc;
     a.rows_per_tile = kDtcM;
     a.row_tiles = (a.m.rows + kDtcM - 1) / kDtcM;
-    const long long grid = std::max(1LL, std::min(tiles_hint, (long long)qmoe::sm_count() * 2));
+    const long long grid = std::max(1LL, std::min(tiles_hint, (long long)qmoe::sm_count()));
     dict_tc_kernel<<<(unsigned)grid, kDtcThreads, kDtcSmem, st>>>(a);
     return qmoe::launch_check("dict_tc_kernel");
 }
@@ -1314,9 +1520,7 @@ MatDev to_dev(const qmoe_matrix_set* s) {
 
 template <bool DICT_SMEM, int NTMAX>
 int launch_gemm_as(const GemmArgs& a, unsigned grid, int threads, size_t smem, cudaStream_t st) {
-    int rc = qmoe::cuda_check(cudaFuncSetAttribute(dict_gemm_kernel<DICT_SMEM, NTMAX>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax),
-                              "cudaFuncSetAttribute");
+    int rc = qmoe::smem_attr((const void*)dict_gemm_kernel<DICT_SMEM, NTMAX>, kSmemMax, "dict gemm attr");
     if (rc) return rc;
     dict_gemm_kernel<DICT_SMEM, NTMAX><<<grid, threads, smem, st>>>(a);
     return QMOE_OK;
@@ -1354,6 +1558,47 @@ int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaS
 
 namespace qmoe {
 
+void* current_context() {
+    using GetCurrent = int (*)(void**);
+    static GetCurrent fn = []() -> GetCurrent {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return (GetCurrent)f;
+    }();
+    void* ctx = nullptr;
+    if (!fn || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
+
+int smem_attr(const void* kernel, int bytes, const char* where) {
+    struct Entry {
+        const void* kernel;
+        int dev;
+        void* ctx;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> set;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    void* ctx = current_context();
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : set)
+        if (ctx && e.kernel == kernel && e.dev == dev && e.ctx == ctx && e.bytes >= bytes) return QMOE_OK;
+    const int rc = cuda_check(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), where);
+    if (rc || !ctx) return rc;
+    for (Entry& e : set)
+        if (e.kernel == kernel && e.dev == dev && e.ctx == ctx) {
+            e.bytes = bytes;
+            return QMOE_OK;
+        }
+    set.push_back({kernel, dev, ctx, bytes});
+    return QMOE_OK;
+}
+
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
@@ -1370,8 +1615,7 @@ int launch_plan(const int32_t* ids, int n_slots, int E, int nt_a, int nt_b, int3
                 Job* jobs_tc) {
     const size_t smem = (size_t)(2 * E + 1) * sizeof(int);
     if (smem > 48 * 1024) {
-        const int rc = cuda_check(cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                                  "plan attr");
+        const int rc = smem_attr((const void*)plan_kernel, (int)smem, "plan attr");
         if (rc) return rc;
     }
     plan_kernel<<<1, kPlanThreads, smem, st>>>(ids, n_slots, E, nt_a, nt_b, tc_min, nt_tc, counts, offsets, perm, jobs_a,
@@ -1423,6 +1667,7 @@ extern "C" int qmoe_expert_matvec(const qmoe_dict* dict, const qmoe_matrix_set* 
     GemmArgs a{};
     a.dictA = (const uint16_t*)dict->compact;
     a.dictB = (const uint8_t*)dict->compact + kDictA;
+    a.dictW = (const uint32_t*)((const uint8_t*)dict->compact + kDictWordsOff);
     a.words = dict->words;
     a.m = to_dev(mat);
     a.x = (const uint16_t*)x_bf16;
@@ -1551,6 +1796,7 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     GemmArgs a{};
     a.dictA = (const uint16_t*)dict->compact;
     a.dictB = (const uint8_t*)dict->compact + kDictA;
+    a.dictW = (const uint32_t*)((const uint8_t*)dict->compact + kDictWordsOff);
     a.words = dict->words;
     a.slots = w.perm;
     a.T_implicit = 0;
@@ -1637,9 +1883,9 @@ extern "C" int qmoe_check_status(void* stream) {
 // this entry point takes its scratch from g_noalloc_scratch, a file-scope
 // device array of kNoAllocScratchBytes that every GPU loading this library
 // holds until the process exits.  The caller still provides inputs and
-// outputs.  The array's address is looked up once per device (with that
-// device current) on the first call made on it; that first call should come
-// before any stream capture.  All calls share the array: calls whose work
+// outputs.  The array's address is looked up once per device and context
+// (with that device current) on the first call made there, and again after a
+// device reset; that first call should come before any stream capture.  All calls share the array: calls whose work
 // overlaps on the GPU (different streams, or different host threads) race on
 // it and must be serialised by the caller.  Nothing in the scratch has to
 // start at zero: every byte a call reads was written earlier in the same call.
@@ -1648,7 +1894,11 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64];
+struct NoAllocAddr {
+    void* ctx;
+    void* ptr;
+};
+NoAllocAddr g_noalloc_addr[64];
 }  // namespace
 
 extern "C" int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_set* wi, const qmoe_matrix_set* wo,
@@ -1656,9 +1906,11 @@ extern "C" int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_s
                                       void* y, int y_is_f32, void* stream) {
     qmoe::clear_error();
     if (!wi || !wo) return fail(QMOE_EINVAL, "qmoe_moe_layer_noalloc: NULL matrix set");
+    if (wi->count < 1 || wi->count > kPlanMaxE || wi->cols < 2 || wi->rows < 2 || T < 0 || k < 1 || k > wi->count)
+        return fail(QMOE_EINVAL, "qmoe_moe_layer_noalloc: bad sizes (E, d_model, d_ff, T or k)");
     size_t need = 0;
     int rc = qmoe_moe_layer_ws_size(wi->count, wi->cols, wi->rows, T, k, &need);
-    if (rc) return rc;
+    if (rc) return fail(rc, "qmoe_moe_layer_noalloc: " + std::string(qmoe_last_error()));
     if (need > kNoAllocScratchBytes)
         return fail(QMOE_ECAPACITY, "qmoe_moe_layer_noalloc: this layer call needs " + std::to_string(need) +
                                         " bytes of scratch; the static scratch holds " +
@@ -1668,17 +1920,22 @@ extern "C" int qmoe_moe_layer_noalloc(const qmoe_dict* dict, const qmoe_matrix_s
     rc = qmoe::cuda_check(cudaGetDevice(&dev), "qmoe_moe_layer_noalloc: cudaGetDevice");
     if (rc) return rc;
     if (dev < 0 || dev >= 64) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer_noalloc: device index above 63");
+    // the array's device address, looked up once per device and context (a device reset or a
+    // caller-created context gets its own lookup)
+    void* const ctx = qmoe::current_context();
     void* ptr = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_noalloc_mu);
-        if (!g_noalloc_ptr[dev]) {
+        NoAllocAddr& c = g_noalloc_addr[dev];
+        if (!c.ptr || !ctx || c.ctx != ctx) {
             void* p = nullptr;
             rc = qmoe::cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch),
                                   "qmoe_moe_layer_noalloc: cudaGetSymbolAddress");
             if (rc) return rc;
-            g_noalloc_ptr[dev] = p;
+            c.ctx = ctx;
+            c.ptr = p;
         }
-        ptr = g_noalloc_ptr[dev];
+        ptr = c.ptr;
     }
     return qmoe_moe_layer(dict, wi, wo, x_bf16, T, k, ids, gates, y, y_is_f32, ptr, kNoAllocScratchBytes, stream);
 }

@@ -246,7 +246,8 @@ extern "C" int qmoe_pack(const int8_t* tern, int rows, int cols, int block,
 }
 
 // ---------------------------------------------------------------------------
-// Compact dictionary: uint16 plane [65536] then uint8 plane [65536];
+// Compact dictionary: uint16 plane [65536], uint8 plane [65536], then both again as one
+// uint32 plane [65536] (uint16 entry | uint8 entry << 16) for reads from global memory;
 // slot = 2*position + (1 if the weight is w_min).
 //   up to three nonzeros:      A [3:0] pair count, [9:4] slot 0, [15:10] slot 1 (63 = empty)
 //                              B [5:0] slot 2 (63 = empty), [7:6] = 0
@@ -260,6 +261,7 @@ extern "C" int qmoe_dict_compact(const uint32_t* dict_words, void* compact) {
     if (!dict_words || !compact) return fail(QMOE_EINVAL, "qmoe_dict_compact: NULL argument");
     uint16_t* pa = (uint16_t*)compact;
     uint8_t* pb = (uint8_t*)compact + 2 * QMOE_DICT_ENTRIES;
+    uint32_t* pw = (uint32_t*)((uint8_t*)compact + 3 * QMOE_DICT_ENTRIES);
     for (int e = 0; e < QMOE_DICT_ENTRIES; ++e) {
         uint32_t w0 = dict_words[2 * e], w1 = dict_words[2 * e + 1];
         uint32_t pairs = w0 & 15u;
@@ -290,6 +292,7 @@ extern "C" int qmoe_dict_compact(const uint32_t* dict_words, void* compact) {
             pa[e] = (uint16_t)(pairs | 0xFFF0u);
             pb[e] = 0xBF;
         }
+        pw[e] = (uint32_t)pa[e] | ((uint32_t)pb[e] << 16);
     }
     return QMOE_OK;
 }

@@ -919,8 +919,7 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
 }
 
 int launch_rvq_tc(RvqGemmArgs a, cudaStream_t st, long long tiles_hint) {
-    int rc = qmoe::cuda_check(
-        cudaFuncSetAttribute(rvq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem), "rvq tc attr");
+    int rc = qmoe::smem_attr((const void*)rvq_tc_kernel, kTcSmem, "rvq tc attr");
     if (rc) return rc;
     a.rows_per_tile = kTcM;
     a.row_tiles = (a.m.rows + kTcM - 1) / kTcM;
@@ -969,8 +968,7 @@ int launch_rvq_gemm(RvqGemmArgs a, cudaStream_t st, long long jobs_hint) {
     const int sms = qmoe::sm_count();
     const size_t tab = a.m.e8p ? (size_t)256 * kE8pRepGemm * 8 : (size_t)a.m.n_st * 256 * 16;
     const size_t smem = tab + (size_t)a.m.cols * a.nt_max * 4;
-    int rc = qmoe::cuda_check(
-        cudaFuncSetAttribute(rvq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem), "rvq attr");
+    int rc = qmoe::smem_attr((const void*)rvq_gemm_kernel, (int)smem, "rvq attr");
     if (rc) return rc;
     int rpt = std::min(a.m.rows, 128);
     while (rpt > 16 && std::max(1LL, jobs_hint) * ((a.m.rows + rpt - 1) / rpt) < 2LL * sms) rpt >>= 1;
@@ -1020,8 +1018,7 @@ int launch_out_transform(const float* yp, const int32_t* expert_of, const int8_t
     }
     const int kg = std::max(1, std::min(k, 98304 / (4 * n) - 1));
     const size_t smem = (size_t)(kg + 1) * n * sizeof(float);
-    int rc = qmoe::cuda_check(cudaFuncSetAttribute(out_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem), "out transform attr");
+    int rc = qmoe::smem_attr((const void*)out_transform_kernel, (int)smem, "out transform attr");
     if (rc) return rc;
     const int threads = std::min(1024, std::max(32, kg * n / 2));
     out_transform_kernel<<<T, threads, smem, st>>>(yp, expert_of, so, gates, k, kg, n, inv_sqrt(n), y, y_is_f32);

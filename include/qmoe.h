@@ -60,7 +60,7 @@ typedef enum {
 #define QMOE_DICT_WORDS (2 * QMOE_DICT_ENTRIES)
 #define QMOE_MAX_RUN 28
 /* bytes of the kernel-private compact dictionary made by qmoe_dict_compact */
-#define QMOE_COMPACT_BYTES (3 * QMOE_DICT_ENTRIES)
+#define QMOE_COMPACT_BYTES (7 * QMOE_DICT_ENTRIES)
 #define QMOE_RVQ_DIM 8
 #define QMOE_RVQ_CODES 256
 /* most residual stages an RVQ code may have */
@@ -131,7 +131,10 @@ int qmoe_pack(const int8_t* tern, int rows, int cols, int block,
  * four 4-bit slots (and a flag) for entries with four nonzeros all in their
  * first eight positions (the four-nonzero entries of dictionaries for
  * p0 >= 0.8); any other entry carries a flag that sends the kernels to its
- * canonical words.  Upload the result
+ * canonical words.  A third plane repeats each entry as one uint32 (the
+ * uint16 entry in bits 0-15, the uint8 entry in bits 16-23) for kernels that
+ * read the table from global memory: one gather per codeword instead of two.
+ * Upload the result
  * next to the canonical words and point qmoe_dict.compact at it.
  *  dict_words host in, QMOE_DICT_WORDS uint32.
  *  compact   host out, QMOE_COMPACT_BYTES bytes.
@@ -274,7 +277,8 @@ int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi,
  * of 16 MiB (16 << 20 bytes) that every GPU loading the library holds until
  * the process exits.
  *  - The first call on a device looks up the array's address on that device
- *    (with that device current); make that first call before any stream
+ *    (with that device current), and looks it up again in another context
+ *    or after a device reset; make that first call before any stream
  *    capture.
  *  - Calls whose needs (qmoe_moe_layer_ws_size) exceed 16 MiB are rejected
  *    with QMOE_ECAPACITY and launch nothing.

@@ -102,7 +102,10 @@ def test_compact_table_lists_every_nonzero(p0):
     words = D.pack(ents)
     comp = Q.qmoe_dict_compact(words)
     plane_a = comp[:2 * 65536].view(np.uint16)
-    plane_b = comp[2 * 65536:]
+    plane_b = comp[2 * 65536:3 * 65536]
+    # the third plane repeats both entries as one uint32
+    plane_w = comp[3 * 65536:7 * 65536].view(np.uint32)
+    assert np.array_equal(plane_w, plane_a.astype(np.uint32) | (plane_b.astype(np.uint32) << 16))
     kinds = set()
     for e, seq in enumerate(ents):
         a, b = int(plane_a[e]), int(plane_b[e])
