@@ -602,6 +602,32 @@ def _dict_layer_row(layer, cfg, T, device, peak, note=""):
             "ms_per_call_cuda_graph": t_graph * 1e3}
 
 
+def _rotating_dict_row(layer, cfg, T, device, peak, replicas=1, batches=1, n=60):
+    """The layer call cycling over `replicas` device copies of the layer's weights (each call streams
+    weights that the previous calls did not leave in L2) or over `batches` token batches (different
+    routing, so mostly different experts): an HBM figure for layers or batches that fit in L2."""
+    import types
+    views = [layer]
+    for _ in range(replicas - 1):
+        views.append(types.SimpleNamespace(dictionary=layer.dictionary, wi=layer.wi_host.to_device(device),
+                                           wo=layer.wo_host.to_device(device), E=layer.E, d_model=layer.d_model,
+                                           d_ff=layer.d_ff))
+    steps = [DictStep(v, cfg, T, b, device) for v in views for b in range(batches)]
+    for st_ in steps:
+        st_.run()
+    calls = [st_.run for st_ in steps]
+    t = _time_calls(lambda it=iter(range(1 << 30)): calls[next(it) % len(calls)](), n=n, warm=len(calls))
+    sb = float(np.mean([layer.stream_bytes(np.unique(st_.ids.cpu().numpy().reshape(-1))) for st_ in steps]))
+    what = f"{replicas} weight copies" if replicas > 1 else f"{batches} token batches"
+    out = {"workload": f"{cfg.name} MoE layer (E={cfg.E}, d={cfg.d_model}, f={cfg.d_ff}, p0={cfg.p0}), T={T}, "
+                       f"cycling over {what}",
+           "tokens_per_s": T / t, "ms_per_call": t * 1e3, "stream_bytes": sb, "stream_gbs": sb / t / 1e9,
+           "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak,
+           "resident_bytes_cycled": sb * len(steps)}
+    del views, steps
+    return out
+
+
 def _graph_time(step, n=50, warm=5):
     """Time of `step` replayed from a CUDA graph (host launch overhead removed)."""
     import torch
@@ -715,12 +741,19 @@ def extra_rows(layer, device, peak):
 
     for T in (64, 1):
         guarded(lambda T=T: _dict_layer_row(layer, CFG, T, device, peak,
-                                            " (L2-resident at T=1: a latency figure)" if T == 1 else ""))
+                                            " (one batch, repeated: L2-resident, a latency figure)" if T == 1 else
+                                            " (one batch, repeated: partly L2-resident)"))
+        # HBM figure: 16 token batches in turn (each call mostly touches experts the last did not)
+        guarded(lambda T=T: _rotating_dict_row(layer, CFG, T, device, peak, batches=16))
     for cfg in (synth.SWITCH_BASE_128, synth.SWITCH_LARGE_128):
         def one(cfg=cfg):
             small = build_dict_layer(cfg, device)
             r = [_dict_layer_row(small, cfg, T, device, peak, " (layer fits in L2: not an HBM figure)")
                  for T in cfg.tokens]
+            # HBM figure: copies of the layer's weights in turn, more than twice the L2 in all
+            per = small.total_bytes()
+            reps = max(2, int(np.ceil(2.2 * 129e6 / per)))
+            r += [_rotating_dict_row(small, cfg, T, device, peak, replicas=reps) for T in cfg.tokens]
             del small
             return r
         guarded(one)
@@ -739,13 +772,24 @@ def extra_rows(layer, device, peak):
         m = Q.MatrixSet.from_host(codes, off, synth.row_scales(lc.seed, 0, 0, lc.rows), lc.rows, lc.cols,
                                   device=device)
         out = []
+        sb = 2 * len(codes) + 4 * len(off) + 2 * lc.rows
+        reps = int(np.ceil(2.2 * 129e6 / sb))
+        copies = [m] + [Q.MatrixSet.from_host(codes, off, synth.row_scales(lc.seed, 0, 0, lc.rows), lc.rows, lc.cols,
+                                              device=device) for _ in range(reps - 1)]
+        peak_ = peak
         for T in lc.tokens:
             x = torch.from_numpy(synth.activations_bf16(lc.seed, T, lc.cols).view(np.int16).copy()).to(device)
             y = torch.empty((T, lc.rows), dtype=torch.int16, device=device)
             t = _time_calls(lambda: Q.qmoe_expert_matvec(d, m, x, y, y_is_f32=False), n=200, warm=10)
-            sb = 2 * len(codes) + 4 * len(off) + 2 * lc.rows
-            out.append({"workload": f"{lc.name}, T={T} (L2-resident: a latency figure)", "tokens_per_s": T / t,
-                        "us_per_call": t * 1e6, "stream_bytes": sb})
+            out.append({"workload": f"{lc.name}, T={T} (one copy, repeated: L2-resident, a latency figure)",
+                        "tokens_per_s": T / t, "us_per_call": t * 1e6, "stream_bytes": sb})
+            it = iter(range(1 << 30))
+            t2 = _time_calls(lambda: Q.qmoe_expert_matvec(d, copies[next(it) % reps], x, y, y_is_f32=False),
+                             n=2 * reps, warm=reps)
+            out.append({"workload": f"{lc.name}, T={T}, cycling over {reps} copies of the matrix ({reps * sb / 1e6:.0f} MB)",
+                        "tokens_per_s": T / t2, "us_per_call": t2 * 1e6, "stream_bytes": sb,
+                        "stream_gbs": sb / t2 / 1e9, "stream_pct_of_hbm_peak": 100.0 * sb / t2 / 1e9 / peak_})
+        del copies
         return out
     guarded(linear)
 
@@ -1006,6 +1050,12 @@ def main():
         kern[name] = {"experts": int(len(ex)), "tokens": n_tok, "launches_per_step": 2,
                       "ms_per_step": secs_k * 1e3, "algorithmic_bytes_per_step": int(b),
                       "achieved_gbs": (b / secs_k / 1e9) if secs_k > 0 else None}
+        if name == "dict_gemm_kernel":
+            # the CUDA-core kernel reads only the row-start offsets, not every block offset
+            nb_i, nb_o = (CFG.d_model + 255) // 256, (CFG.d_ff + 255) // 256
+            unread = len(ex) * 4 * (CFG.d_ff * (nb_i - 1) + CFG.d_model * (nb_o - 1))
+            kern[name]["bytes_read_per_step"] = int(b - unread)
+            kern[name]["achieved_gbs_on_bytes_read"] = (b - unread) / secs_k / 1e9 if secs_k > 0 else None
     dom = max(kern, key=lambda k: kern[k]["ms_per_step"])
     peak, peak_kind = hbm_peak()
     achieved = kern[dom]["achieved_gbs"]
@@ -1033,6 +1083,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_kind": "measured (MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": achieved / peak,
+                     "frac_on_bytes_read": (kern[dom].get("achieved_gbs_on_bytes_read") or achieved) / peak,
                      "traffic": kernel_traffic("decode_matvec_gb300/csrc/dict_kernels.cu", dom),
                      "kernels": kern, "phase_ms": {k: v * 1e3 for k, v in phases.items()}},
         "e2e": {"value": T_MAIN / e2e_s, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo},
