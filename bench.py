@@ -42,7 +42,8 @@ import synth  # noqa: E402
 
 CFG = synth.SWITCH_C2048
 T_MAIN = 4096
-TC_MIN_TOKENS = 32      # experts with this many tokens take the tensor-core kernel
+TC_MIN_TOKENS = 32      # experts with this many tokens take the tensor-core kernel ...
+TC_MIN_SLOTS = 256      # ... in launches with at least this many token slots
 METRIC = "MoE-layer tokens/s and compressed-stream HBM GB/s (% of GB300 peak) at 1 GPU"
 UNIT = "tokens/s"
 WORKLOAD = (f"{CFG.name} MoE FFN layer: E={CFG.E}, d_model={CFG.d_model}, d_ff={CFG.d_ff}, T={T_MAIN} bf16 tokens, "
@@ -1039,7 +1040,7 @@ def main():
     stream_bytes = layer.stream_bytes(touched)
     counts = np.bincount(ids, minlength=CFG.E)
     # experts with >= 32 tokens run on the tensor-core kernel (large launches only)
-    hot = counts >= TC_MIN_TOKENS if T_MAIN >= TC_MIN_TOKENS else np.zeros(CFG.E, bool)
+    hot = counts >= TC_MIN_TOKENS if T_MAIN >= TC_MIN_SLOTS else np.zeros(CFG.E, bool)
     kern = {}
     for name, sel, secs_k in (("dict_gemm_kernel", (counts > 0) & ~hot, phases["wi"] + phases["wo"]),
                               ("dict_tc_kernel", hot, phases["wi_tc"] + phases["wo_tc"])):

@@ -51,6 +51,10 @@ constexpr int kSaccBytes = 8192;                                // per-tile row 
 #define QMOE_SACC_SMALL_SLOTS 1024
 #endif
 constexpr int kTcMinTokens = 32;                                // experts this busy use the tensor-core kernel
+#ifndef QMOE_TC_MIN_SLOTS
+#define QMOE_TC_MIN_SLOTS 256
+#endif
+constexpr int kTcMinSlots = QMOE_TC_MIN_SLOTS;                 // ... in launches with at least this many slots
 // Threads of a block with the dictionary in SMEM, by the launch's largest
 // token class: fewer accumulators per thread leave registers for more warps,
 // which hide more of the shared-memory gather latency (measured on the
@@ -1770,7 +1774,12 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     MoeWs w = moe_ws_layout(workspace, E, d_model, d_ff, T, k);
     if (ws_bytes < w.bytes) return fail(QMOE_ECAPACITY, "qmoe_moe_layer: workspace too small");
     const long long slots = (long long)T * k;
-    const bool big = slots >= 16;
+    // launches with this many token slots stage the compact dictionary in shared memory; smaller
+    // ones read it through L1/L2
+#ifndef QMOE_SMEM_DICT_MIN_SLOTS
+#define QMOE_SMEM_DICT_MIN_SLOTS 16
+#endif
+    const bool big = slots >= QMOE_SMEM_DICT_MIN_SLOTS;
     const int budget = big ? kBudgetSmemDict : kBudgetGlobalDict;
     const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
     const int nw_wi = (big ? threads_smem_dict(nt_wi) : kThreadsGlobalDict) / 32;
@@ -1787,7 +1796,9 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer: d_model or d_ff too large");
     cudaStream_t st = (cudaStream_t)stream;
     // experts with at least kTcMinTokens tokens take the tensor-core kernel
-    const bool use_tc = big && slots >= kTcMinTokens && d_model % 8 == 0 && d_ff % 8 == 0;
+    // (below kTcMinSlots token slots every expert takes the CUDA-core kernel: an expert of such a
+    // batch rarely reaches kTcMinTokens, and an empty tensor-core launch costs a few microseconds)
+    const bool use_tc = big && slots >= kTcMinSlots && d_model % 8 == 0 && d_ff % 8 == 0;
     qmoe::phase_event(0, st);
     int rc = qmoe::launch_plan(ids, (int)slots, E, nt_wi, nt_wo, w.counts, w.offsets, w.perm, w.jobs_a, w.jobs_b,
                                w.n_jobs, st, use_tc ? kTcMinTokens : 0, kDtcN, use_tc ? w.jobs_tc : nullptr);

@@ -195,15 +195,16 @@ def test_c2048_full_shape_t4096(dev, c2048):
 
 
 def test_c2048_shaped_token_counts_around_tensor_core_threshold(dev):
-    """Four c2048-shaped experts (d_model 2080, d_ff 6144) with 31, 32, 33 and 3 tokens routed by
-    hand (T = 99, k = 1): the tensor-core threshold from both sides, several-token chunks with odd
-    remainders on the CUDA-core kernel (wi and wo token classes of the full-size layer)."""
+    """Six c2048-shaped experts (d_model 2080, d_ff 6144) with 31, 32, 33, 3, 150 and 7 tokens routed
+    by hand (T = 256, k = 1, enough slots for the tensor-core kernel): its threshold from both sides,
+    a 150-token expert split into several tensor-core jobs, several-token chunks with odd remainders
+    on the CUDA-core kernel (wi and wo token classes of the full-size layer)."""
     cfg = synth.SWITCH_C2048
     import dataclasses
-    small = dataclasses.replace(cfg, E=4)
+    small = dataclasses.replace(cfg, E=6)
     layer = build_dict_layer(small, dev)
     experts = SeededExperts(small)
-    counts = [31, 32, 33, 3]
+    counts = [31, 32, 33, 3, 150, 7]
     rid = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(counts)])
     rid = rid[np.random.default_rng(5).permutation(rid.size)].reshape(-1, 1)
     rg = np.random.default_rng(6).uniform(0.2, 1.0, size=rid.shape)
@@ -241,8 +242,9 @@ def test_degenerate_experts_in_a_layer_call(dev, p0):
         return t * synth.f16_to_f64(synth.row_scales(cfg.seed, e, m, rows))[:, None]
 
     experts = SeededExperts(cfg, weights)
-    # each degenerate expert once on the tensor-core kernel (40 tokens) and once on the CUDA-core one
-    for counts in ((40, 5, 1), (5, 40, 1)):
+    # each degenerate expert once on the tensor-core kernel (200 tokens) and once on the CUDA-core one
+    # (256 slots: enough for the tensor-core kernel to run)
+    for counts in ((200, 5, 51), (5, 200, 51)):
         rid = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(counts)])
         rid = rid[np.random.default_rng(7).permutation(rid.size)].reshape(-1, 1)
         rg = np.ones(rid.shape, np.float32)
