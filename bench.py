@@ -3,8 +3,9 @@
 
 One step = one pass of the dictionary-path hot path over one token batch of
 the switch-c2048-shaped MoE FFN layer (E=2048 experts, d_model=2080,
-d_ff=6144, ternary weights with P(0)=0.886 dictionary-coded at ~0.76 bits per
-weight, T=4096 bf16 tokens, top-1 Zipf(1.0) routing): route (top-1 + softmax
+d_ff=6144, ternary weights with P(0)=0.886 dictionary-coded: ~0.76 bits per
+weight of codewords, ~0.82 stored with row starts, block lengths and row
+scales; T=4096 bf16 tokens, top-1 Zipf(1.0) routing): route (top-1 + softmax
 gate) -> bucket tokens by expert -> fused decode-multiply of every touched
 expert's wi with ReLU -> fused decode-multiply of wo with the gate applied.
 Inputs are resident in HBM; each step streams the touched experts' compressed
@@ -827,14 +828,7 @@ def extra_rows(layer, device, peak):
 
 def _expert_view(Q, ms, host, e):
     """A count-1 matrix descriptor for expert e of a device matrix set."""
-    import ctypes
-    nb = (ms.cols + ms.block - 1) // ms.block
-    base = int(host.code_base[e])
-    c = Q.CMatrixSet(ms.codes.data_ptr() + 2 * base, None, ms.blk_off.data_ptr() + 4 * e * (ms.rows * nb + 1),
-                     ms.scale.data_ptr() + 2 * e * ms.rows, 1, ms.rows, ms.cols, ms.block)
-    view = type("ExpertView", (), {})()
-    view.c = c
-    return view
+    return ms.expert(e, host.code_base)
 
 
 def _materialise_row(layer, device, T):
@@ -1052,9 +1046,9 @@ def main():
                       "ms_per_step": secs_k * 1e3, "algorithmic_bytes_per_step": int(b),
                       "achieved_gbs": (b / secs_k / 1e9) if secs_k > 0 else None}
         if name == "dict_gemm_kernel":
-            # the CUDA-core kernel reads only the row-start offsets, not every block offset
-            nb_i, nb_o = (CFG.d_model + 255) // 256, (CFG.d_ff + 255) // 256
-            unread = len(ex) * 4 * (CFG.d_ff * (nb_i - 1) + CFG.d_model * (nb_o - 1))
+            # the CUDA-core kernel reads only the row starts, not the block lengths
+            unread = sum(layer.wi_host.expert_offset_bytes_unread_by_cuda_cores(int(e)) +
+                         layer.wo_host.expert_offset_bytes_unread_by_cuda_cores(int(e)) for e in ex)
             kern[name]["bytes_read_per_step"] = int(b - unread)
             kern[name]["achieved_gbs_on_bytes_read"] = (b - unread) / secs_k / 1e9 if secs_k > 0 else None
     dom = max(kern, key=lambda k: kern[k]["ms_per_step"])

@@ -34,7 +34,7 @@ EXPORTED = [
     "rvq_expert_matmul", "rvq_moe_layer_ws_size", "rvq_moe_layer", "rvq_pack", "qmoe_check_status",
     "qmoe_last_error", "qmoe_decode_dense", "rvq_decode_dense", "qmoe_set_phase_events",
     "qmoe_moe_layer_noalloc", "qmoe_pack_device_ws_size", "qmoe_pack_device", "rvq_pack_stages",
-    "rvq_stage_allocation", "e8p_base_table", "e8p_pack", "e8p_nearest",
+    "rvq_stage_allocation", "e8p_base_table", "e8p_pack", "e8p_nearest", "qmoe_offsets_compact",
 ]
 
 
@@ -56,7 +56,8 @@ class CDict(ctypes.Structure):
 
 
 class CMatrixSet(ctypes.Structure):
-    _fields_ = [("codes", ctypes.c_void_p), ("code_base", ctypes.c_void_p), ("blk_off", ctypes.c_void_p),
+    _fields_ = [("codes", ctypes.c_void_p), ("code_base", ctypes.c_void_p), ("row_off", ctypes.c_void_p),
+                ("blk_len", ctypes.c_void_p),
                 ("scale_f16", ctypes.c_void_p), ("count", ctypes.c_int), ("rows", ctypes.c_int),
                 ("cols", ctypes.c_int), ("block", ctypes.c_int)]
 
@@ -95,6 +96,7 @@ _sig = {
     "e8p_base_table": [_vp],
     "e8p_pack": [_vp, _i, _i, _vp, _vp, _vp, _vp],
     "e8p_nearest": [_vp, _sz, _vp],
+    "qmoe_offsets_compact": [_vp, _i, _i, _vp, _vp],
 }
 for _name, _args in _sig.items():
     _f = getattr(_lib, _name)
@@ -246,28 +248,57 @@ class Dictionary:
 
 
 class MatrixSet:
-    """`count` dictionary-coded matrices of one shape, resident on the device."""
+    """`count` dictionary-coded matrices of one shape, resident on the device, with compact offsets:
+    row_off uint32 [count][rows + 1] and blk_len uint8 [count][rows][nb - 1] (qmoe_offsets_compact)."""
 
-    def __init__(self, codes, code_base, blk_off, scale_f16, count, rows, cols, block=256):
-        self.codes, self.code_base, self.blk_off, self.scale = codes, code_base, blk_off, scale_f16
+    def __init__(self, codes, code_base, row_off, blk_len, scale_f16, count, rows, cols, block=256):
+        self.codes, self.code_base, self.row_off, self.blk_len, self.scale = codes, code_base, row_off, blk_len, scale_f16
         self.count, self.rows, self.cols, self.block = count, rows, cols, block
-        self.c = CMatrixSet(_dptr(codes), _dptr(code_base), _dptr(blk_off), _dptr(scale_f16), count, rows, cols,
-                            block)
+        self.c = CMatrixSet(_dptr(codes), _dptr(code_base), _dptr(row_off), _dptr(blk_len), _dptr(scale_f16), count,
+                            rows, cols, block)
+
+    @property
+    def nb(self) -> int:
+        return (self.cols + self.block - 1) // self.block
 
     @classmethod
     def from_host(cls, codes: np.ndarray, blk_off: np.ndarray, scale_f16: np.ndarray, rows, cols, block=256,
                   code_base: np.ndarray | None = None, count: int = 1, device="cuda"):
+        """From qmoe_pack's output (uint32 block offsets [count][rows*nb + 1]), re-encoded compactly."""
         import torch
         codes = np.ascontiguousarray(codes, dtype=np.uint16)
         padded = np.zeros((codes.size + 15) // 8 * 8, dtype=np.uint16)     # whole 16-byte chunks, plus one
         padded[:codes.size] = codes
         c = torch.from_numpy(padded.view(np.int16)).to(device)
-        o = torch.from_numpy(np.ascontiguousarray(blk_off, dtype=np.uint32).view(np.int32).copy()).to(device)
+        row_off, blk_len = qmoe_offsets_compact(blk_off, rows, (cols + block - 1) // block, count)
+        o = torch.from_numpy(row_off.view(np.int32).copy()).to(device)
+        bl = torch.from_numpy(blk_len.copy()).to(device) if blk_len.size else None
         s = torch.from_numpy(np.ascontiguousarray(scale_f16, dtype=np.uint16).view(np.int16).copy()).to(device)
         b = None
         if code_base is not None:
             b = torch.from_numpy(np.ascontiguousarray(code_base, dtype=np.uint64).view(np.int64).copy()).to(device)
-        return cls(c, b, o, s, count, rows, cols, block)
+        return cls(c, b, o, bl, s, count, rows, cols, block)
+
+    def expert(self, e: int, code_base_host=None) -> "MatrixSet":
+        """A one-matrix set for matrix e (views into the same device buffers); code_base_host: the host copy
+        of the set's code bases (needed when count > 1)."""
+        base = int(code_base_host[e]) if self.count > 1 else 0
+        nb1 = self.nb - 1
+        return MatrixSet(self.codes[base:], None, self.row_off[e * (self.rows + 1):(e + 1) * (self.rows + 1)],
+                         self.blk_len[e * self.rows * nb1:(e + 1) * self.rows * nb1] if nb1 else None,
+                         self.scale[e * self.rows:(e + 1) * self.rows], 1, self.rows, self.cols, self.block)
+
+
+def qmoe_offsets_compact(blk_off: np.ndarray, rows: int, nb: int, count: int = 1):
+    """Compact offsets of `count` matrices from their uint32 block offsets [count][rows*nb + 1]:
+    (row_off uint32 [count*(rows + 1)], blk_len uint8 [count*rows*(nb - 1)])."""
+    bo = np.ascontiguousarray(blk_off, dtype=np.uint32).reshape(count, rows * nb + 1)
+    row_off = np.zeros((count, rows + 1), dtype=np.uint32)
+    blk_len = np.zeros((count, rows * (nb - 1)), dtype=np.uint8)
+    for e in range(count):
+        _check(_lib.qmoe_offsets_compact(_np_ptr(bo[e]), rows, nb, _np_ptr(row_off[e]),
+                                         _np_ptr(blk_len[e]) if nb > 1 else None), "qmoe_offsets_compact")
+    return row_off.reshape(-1), blk_len.reshape(-1)
 
 
 class RvqMatrixSet:

@@ -82,7 +82,8 @@ constexpr int kThreadsGlobalDict = 256;
 struct MatDev {
     const uint16_t* codes;
     const uint64_t* code_base;
-    const uint32_t* blk_off;
+    const uint32_t* row_off;     // [count][rows + 1]
+    const uint8_t* blk_len;      // [count][rows][nb - 1]
     const uint16_t* scale;
     int count, rows, cols, block, nb;
 };
@@ -537,10 +538,10 @@ __device__ void prefetch_tile(const GemmArgs& a, int tile, int n_tiles) {
     int r0, r1;
     tile_rows_of(a, tile, job, r0, r1);
     const MatDev& m = a.m;
-    const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
+    const uint32_t* ro = m.row_off + (size_t)job.matrix * (m.rows + 1);
     const uint64_t base = m.code_base ? m.code_base[job.matrix] : 0ull;
-    const uint64_t lo = (base + off[(size_t)r0 * m.nb]) & ~7ull;
-    const uint64_t hi = (base + off[(size_t)r1 * m.nb] + 7) & ~7ull;
+    const uint64_t lo = (base + ro[r0]) & ~7ull;
+    const uint64_t hi = (base + ro[r1] + 7) & ~7ull;
     if (hi <= lo) return;
     const char* p = (const char*)(m.codes + lo);
     uint64_t bytes = (hi - lo) * 2;
@@ -560,12 +561,12 @@ __device__ void run_tile(const GemmArgs& a, const SmemMap& sm, const Job& job, i
     const int nr = r1 - r0;
     for (int i = tid; i < nr * NT; i += nthreads) ((float*)(g_smem + sm.sacc))[i] = 0.0f;
     __syncthreads();
-    const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * m.nb + 1);
+    const uint32_t* ro = m.row_off + (size_t)job.matrix * (m.rows + 1);
     const uint64_t base = m.code_base ? m.code_base[job.matrix] : 0ull;
     const int per = (nr + nwarps - 1) / nwarps;
     const int wr0 = r0 + warp * per, wr1 = min(r1, wr0 + per);
     if (wr0 < wr1) {
-        const uint32_t lo = off[(size_t)wr0 * m.nb], hi = off[(size_t)wr1 * m.nb];
+        const uint32_t lo = ro[wr0], hi = ro[wr1];
         if (hi < lo) {
             if (lane == 0) set_error(QMOE_EFORMAT);
         } else {
@@ -759,11 +760,6 @@ __device__ __forceinline__ RowBlk load_rowblk(const uint16_t* codes, uint2 range
     return p;
 }
 
-// Start and end codeword of block b of a row (relative to the expert's base).
-__device__ __forceinline__ uint2 load_range(const uint32_t* off_row, int b) {
-    return make_uint2(__ldg(off_row + b), __ldg(off_row + b + 1));
-}
-
 // One thread expands the codewords of one (row, block) into the tile row `rl`
 // (bf16 +-1 at the nonzeros of an already zeroed row).  The codewords come 16 at
 // a time as two aligned 16-byte chunks (the first two preloaded); the 16 compact
@@ -919,22 +915,42 @@ __global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs 
             const Job job = a.jobs[tile / a.row_tiles];
             const int row = (tile % a.row_tiles) * kDtcM + rl;
             const bool live = row < m.rows;
-            const uint32_t* off = m.blk_off + (size_t)job.matrix * ((size_t)m.rows * nb + 1) + (size_t)row * nb;
+            const uint32_t* ro = m.row_off + (size_t)job.matrix * (m.rows + 1);
+            const uint8_t* bl = m.blk_len + ((size_t)job.matrix * m.rows + (live ? row : 0)) * (nb - 1);
             const uint64_t cbase = m.code_base ? m.code_base[job.matrix] : 0ull;
             // the group's blocks of the tile are b_first, b_first + 2, ...; the memory reads run ahead of
-            // the decoding: a block's codeword range two of the group's blocks ahead, its first codewords
-            // one ahead, so that decoding a block waits only for its dictionary entries
+            // the decoding: the block lengths that give a block's codeword range three of the group's
+            // blocks ahead, the range two ahead, its first codewords one ahead, so that decoding a block
+            // waits only for its dictionary entries.  Block b < nb - 1 has a stored length; the last
+            // block ends at the row end.
             const int b_first = (int)((group - (int)(gb & 1u)) & 1);
             const uint2 z2 = make_uint2(0u, 0u);
-            const uint2 r_first = live && b_first < nb ? load_range(off, b_first) : z2;
-            uint2 r_ahead = live && b_first + 2 < nb ? load_range(off, b_first + 2) : z2;
+            uint32_t re = 0, pl1 = 0, pl2 = 0;
+            uint2 r_cur = z2, r_ahead = z2;
             RowBlk cur{};
-            if (live && b_first < nb) cur = load_rowblk(m.codes, r_first, cbase, min(kDtcK, m.cols - b_first * kDtcK));
+            if (live && b_first < nb) {
+                const uint32_t rs = __ldg(ro + row);
+                re = __ldg(ro + row + 1);
+                const uint32_t s0 = rs + (b_first == 1 ? (uint32_t)__ldg(bl) : 0u);
+                r_cur = make_uint2(s0, b_first < nb - 1 ? s0 + __ldg(bl + b_first) : re);
+                if (b_first + 2 < nb) {
+                    const uint32_t s2 = r_cur.y + __ldg(bl + b_first + 1);
+                    r_ahead = make_uint2(s2, b_first + 2 < nb - 1 ? s2 + __ldg(bl + b_first + 2) : re);
+                }
+                pl1 = b_first + 4 < nb ? __ldg(bl + b_first + 3) : 0u;
+                pl2 = b_first + 4 < nb - 1 ? __ldg(bl + b_first + 4) : 0u;
+                cur = load_rowblk(m.codes, r_cur, cbase, min(kDtcK, m.cols - b_first * kDtcK));
+            }
             for (int b = 0; b < nb; ++b, ++gb) {
                 if ((int)(gb & 1u) != group) continue;
                 RowBlk nxt{};
-                if (live && b + 2 < nb) nxt = load_rowblk(m.codes, r_ahead, cbase, min(kDtcK, m.cols - (b + 2) * kDtcK));
-                r_ahead = live && b + 4 < nb ? load_range(off, b + 4) : z2;
+                if (live && b + 2 < nb) {
+                    nxt = load_rowblk(m.codes, r_ahead, cbase, min(kDtcK, m.cols - (b + 2) * kDtcK));
+                    const uint32_t s4 = r_ahead.y + pl1;
+                    r_ahead = b + 4 < nb ? make_uint2(s4, b + 4 < nb - 1 ? s4 + pl2 : re) : z2;
+                    pl1 = b + 6 < nb ? __ldg(bl + b + 5) : 0u;
+                    pl2 = b + 6 < nb - 1 ? __ldg(bl + b + 6) : 0u;
+                }
                 if (!mbar_wait_sleep(empty_a + group, ((gb >> 1) & 1u) ^ 1u, kDtcSpin) || *abort_v) {
                     timed_out = true;
                     break;
@@ -1106,7 +1122,14 @@ __global__ void decode_dense_kernel(const uint32_t* __restrict__ words, MatDev m
     float* o = out + (size_t)r * m.cols + c0;
     for (int p = lane; p < blen; p += 32) o[p] = 0.0f;
     __syncwarp();
-    const uint32_t lo = m.blk_off[(size_t)r * m.nb + b], hi = m.blk_off[(size_t)r * m.nb + b + 1];
+    // block b starts after the stored lengths of blocks 0 .. b-1 of the row; the last block ends at the
+    // row end
+    const uint8_t* bl = m.blk_len + (size_t)r * (m.nb - 1);
+    uint32_t pre = 0;
+    for (int j = lane; j < b; j += 32) pre += bl[j];
+    pre = (uint32_t)warp_sum_int((int)pre);
+    const uint32_t lo = m.row_off[r] + pre;
+    const uint32_t hi = b < m.nb - 1 ? lo + bl[b] : m.row_off[r + 1];
     const float s = f16_to_f32(m.scale[r]);
     bool bad = hi < lo;
     int base = 0;
@@ -1504,15 +1527,19 @@ int rows_per_tile_for(int rows, int nt, int nwarps, long long n_jobs, long long 
 }
 
 bool valid_set(const qmoe_matrix_set* s) {
-    return s && s->codes && s->blk_off && s->scale_f16 && s->count >= 1 && s->rows >= 1 && s->cols >= 2 &&
-           (s->cols % 2) == 0 && s->block >= 2 && (s->block % 2) == 0 && (s->count == 1 || s->code_base);
+    if (!s || !s->codes || !s->row_off || !s->scale_f16 || s->count < 1 || s->rows < 1 || s->cols < 2 ||
+        (s->cols % 2) != 0 || s->block < 2 || (s->block % 2) != 0 || s->block > 510 || (s->count > 1 && !s->code_base))
+        return false;
+    const int nb = (s->cols + s->block - 1) / s->block;
+    return nb == 1 || s->blk_len;
 }
 
 MatDev to_dev(const qmoe_matrix_set* s) {
     MatDev m;
     m.codes = s->codes;
     m.code_base = s->code_base;
-    m.blk_off = s->blk_off;
+    m.row_off = s->row_off;
+    m.blk_len = s->blk_len;
     m.scale = s->scale_f16;
     m.count = s->count;
     m.rows = s->rows;

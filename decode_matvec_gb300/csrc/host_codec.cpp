@@ -246,6 +246,27 @@ extern "C" int qmoe_pack(const int8_t* tern, int rows, int cols, int block,
 }
 
 // ---------------------------------------------------------------------------
+// Compact block offsets: per-row uint32 starts and per-block uint8 codeword counts
+// ---------------------------------------------------------------------------
+extern "C" int qmoe_offsets_compact(const uint32_t* blk_off, int rows, int nb, uint32_t* row_off, uint8_t* blk_len) {
+    qmoe::clear_error();
+    if (!blk_off || !row_off || rows < 1 || nb < 1 || (nb > 1 && !blk_len))
+        return fail(QMOE_EINVAL, "qmoe_offsets_compact: bad arguments");
+    if (blk_off[0] != 0) return fail(QMOE_EFORMAT, "qmoe_offsets_compact: offsets must start at 0");
+    for (int r = 0; r < rows; ++r) {
+        const uint32_t* o = blk_off + (size_t)r * nb;
+        row_off[r] = o[0];
+        for (int b = 0; b < nb; ++b) {
+            if (o[b + 1] < o[b]) return fail(QMOE_EFORMAT, "qmoe_offsets_compact: offsets decrease");
+            if (o[b + 1] - o[b] > 255u) return fail(QMOE_EFORMAT, "qmoe_offsets_compact: a block of more than 255 codewords");
+            if (b < nb - 1) blk_len[(size_t)r * (nb - 1) + b] = (uint8_t)(o[b + 1] - o[b]);
+        }
+    }
+    row_off[rows] = blk_off[(size_t)rows * nb];
+    return QMOE_OK;
+}
+
+// ---------------------------------------------------------------------------
 // Compact dictionary: uint16 plane [65536], uint8 plane [65536], then both again as one
 // uint32 plane [65536] (uint16 entry | uint8 entry << 16) for reads from global memory;
 // slot = 2*position + (1 if the weight is w_min).

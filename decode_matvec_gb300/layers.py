@@ -38,8 +38,13 @@ class DictLayerArtifact:
         return (self.cols + self.block - 1) // self.block
 
     def expert_bytes(self, e: int) -> int:
-        """Stored bytes of matrix e: codes + block offsets + scales."""
-        return 2 * int(self.n_codes[e]) + 4 * (self.rows * self.nb + 1) + 2 * self.rows
+        """Stored bytes of matrix e as the device holds it: codes (uint16), row starts (uint32, rows + 1),
+        block lengths (uint8, rows x (nb - 1)) and row scales (fp16)."""
+        return 2 * int(self.n_codes[e]) + 4 * (self.rows + 1) + self.rows * (self.nb - 1) + 2 * self.rows
+
+    def expert_offset_bytes_unread_by_cuda_cores(self, e: int) -> int:
+        """The block lengths of matrix e: the CUDA-core kernel reads only the row starts."""
+        return self.rows * (self.nb - 1)
 
     def to_device(self, device="cuda") -> MatrixSet:
         return MatrixSet.from_host(self.codes, self.blk_off, self.scales, self.rows, self.cols, self.block,

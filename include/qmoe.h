@@ -185,24 +185,47 @@ int qmoe_pack_device(const qmoe_dict* dict, const int8_t* tern, int rows, int co
 
 /*
  * `count` dictionary-coded matrices of the same shape (e.g. the wi matrices
- * of all experts of a layer).  Matrix e's codewords start at
- * codes[code_base[e]]; its block offsets are blk_off[e*(rows*nb+1) + ...],
- * relative to code_base[e], nb = ceil(cols/block); its scales are
+ * of all experts of a layer), with their block offsets stored compactly (a
+ * re-encoding of qmoe_pack's uint32 offsets that qmoe_offsets_compact
+ * makes; the rate ledger counts these stored widths):
+ *  - row_off[e*(rows+1) + r]: index of the first codeword of row r of matrix
+ *    e, relative to code_base[e]; row_off[e*(rows+1) + rows] = its codeword
+ *    count.  uint32.
+ *  - blk_len[(e*rows + r)*(nb-1) + b], b < nb-1: the number of codewords of
+ *    block b of row r (the last block's count is what the row leaves),
+ *    nb = ceil(cols/block).  uint8: a block holds at most block/2 <= 255
+ *    codewords, so block <= 510.
+ * Matrix e's codewords start at codes[code_base[e]]; its scales are
  * scale_f16[e*rows + r].  code_base may be NULL when count == 1 (base 0).
  * The kernels read codewords in aligned 16-byte chunks: `codes` must be
  * 16-byte aligned and its allocation must extend (zero-padded) to the next
  * multiple of 8 codewords after the last codeword of the set.  Offsets must
- * lie inside the codes allocation; the kernels check that each row expands to
- * exactly `cols` weights (QMOE_EFORMAT otherwise) but cannot check offsets
- * against the allocation size.
+ * lie inside the codes allocation; the kernels check that each row and each
+ * block expands to exactly its length (QMOE_EFORMAT otherwise) but cannot
+ * check offsets against the allocation size.
  */
 typedef struct {
     const uint16_t* codes;      /* device */
     const uint64_t* code_base;  /* device [count], or NULL when count == 1 */
-    const uint32_t* blk_off;    /* device [count][rows*nb + 1] */
+    const uint32_t* row_off;    /* device [count][rows + 1] */
+    const uint8_t* blk_len;     /* device [count][rows][nb - 1] (NULL when nb == 1) */
     const uint16_t* scale_f16;  /* device [count][rows] fp16 bits */
     int count, rows, cols, block;
 } qmoe_matrix_set;
+
+/*
+ * The compact offsets of qmoe_matrix_set from qmoe_pack's (or the device
+ * encoder's) block offsets of one matrix: row_off[r] = blk_off[r*nb],
+ * row_off[rows] = blk_off[rows*nb]; blk_len[r*(nb-1) + b] =
+ * blk_off[r*nb + b + 1] - blk_off[r*nb + b] for b < nb-1.
+ *  blk_off  host in uint32 [rows*nb + 1], non-decreasing from 0.
+ *  row_off  host out uint32 [rows + 1];  blk_len host out uint8
+ *           [rows*(nb-1)] (may be NULL when nb == 1).
+ * Errors: EINVAL (null pointer, rows < 1, nb < 1), EFORMAT (offsets that
+ * decrease, do not start at 0, or a block of more than 255 codewords).
+ */
+int qmoe_offsets_compact(const uint32_t* blk_off, int rows, int nb,
+                         uint32_t* row_off, uint8_t* blk_len);
 
 /* ======================================================================
  * Dictionary path: fused decode-and-multiply

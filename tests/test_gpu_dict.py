@@ -149,7 +149,7 @@ def test_corrupt_stream_reports_format_error(dev, dict886):
 def test_bad_arguments_rejected_on_host(dev, dict886):
     tern, codes, off, scale = oracle_matrix(9, 0, 0, 4, 64, 0.886)
     m = _single(codes, off, scale, 4, 64)
-    bad = Q.MatrixSet(m.codes, None, m.blk_off, m.scale, 1, 4, 63, 256)
+    bad = Q.MatrixSet(m.codes, None, m.row_off, m.blk_len, m.scale, 1, 4, 63, 256)
     y = torch.empty((1, 4), dtype=torch.float32, device=dev)
     with pytest.raises(Q.QmoeError):
         Q.qmoe_expert_matvec(dict886, bad, bf16_tensor(synth.activations_bf16(1, 1, 64)), y)

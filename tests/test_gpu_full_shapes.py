@@ -56,11 +56,7 @@ def build_dict_layer(cfg, dev, tern_fns=None):
 
 def expert_view(ms, host, e):
     """A one-matrix set for expert e of a device matrix set (views into the same buffers)."""
-    nb = (ms.cols + ms.block - 1) // ms.block
-    base = int(host.code_base[e])
-    n_off = ms.rows * nb + 1
-    return Q.MatrixSet(ms.codes[base:], None, ms.blk_off[e * n_off:(e + 1) * n_off],
-                       ms.scale[e * ms.rows:(e + 1) * ms.rows], 1, ms.rows, ms.cols, ms.block)
+    return ms.expert(e, host.code_base)
 
 
 class SeededExperts:

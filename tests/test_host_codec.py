@@ -246,3 +246,32 @@ def test_e8p_pack_rejects_bad_inputs():
     with pytest.raises(Q.QmoeError):
         Q.e8p_pack(np.zeros((16, 64)), so, si)             # a zero row has no scale
     assert Q.e8p_nearest(np.zeros((0, 8))).shape == (0,)
+
+
+def test_offsets_compact_round_trip(words886):
+    # the device layout's row starts and per-block codeword counts re-encode qmoe_pack's offsets exactly
+    tern = synth.ternary_matrix(4, 0, 0, 37, 1030, 0.886)
+    codes, off = Q.qmoe_pack(tern, words886)
+    nb = (1030 + 255) // 256
+    row_off, blk_len = Q.qmoe_offsets_compact(off, 37, nb)
+    assert row_off.dtype == np.uint32 and blk_len.dtype == np.uint8
+    assert row_off.size == 38 and blk_len.size == 37 * (nb - 1)
+    rebuilt = np.zeros_like(off)
+    for r in range(37):
+        starts = row_off[r] + np.concatenate([[0], np.cumsum(blk_len[r * (nb - 1):(r + 1) * (nb - 1)])])
+        rebuilt[r * nb:(r + 1) * nb] = starts
+    rebuilt[-1] = row_off[-1]
+    assert np.array_equal(rebuilt, off)
+    # two matrices back to back
+    ro2, bl2 = Q.qmoe_offsets_compact(np.concatenate([off, off]), 37, nb, count=2)
+    assert np.array_equal(ro2[:38], row_off) and np.array_equal(ro2[38:], row_off)
+    assert np.array_equal(bl2[:blk_len.size], blk_len)
+
+
+def test_offsets_compact_rejects_bad_offsets():
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_offsets_compact(np.array([0, 5, 3, 8], np.uint32), 1, 3)          # decreasing
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_offsets_compact(np.array([0, 300, 310], np.uint32), 1, 2)         # a block of 300 codewords
+    with pytest.raises(Q.QmoeError):
+        Q.qmoe_offsets_compact(np.array([1, 5, 9], np.uint32), 1, 2)             # not starting at 0
