@@ -596,12 +596,13 @@ def _dict_layer_row(layer, cfg, T, device, peak, note=""):
     st = DictStep(layer, cfg, T, 0, device)
     t = _time_calls(st.run)
     t_graph = _graph_time(st.run)
+    phases = {k: v * 1e3 for k, v in time_phases(st, 20).items()}
     touched = np.unique(st.ids.cpu().numpy().reshape(-1))
     sb = layer.stream_bytes(touched)
     return {"workload": f"{cfg.name} MoE layer (E={cfg.E}, d={cfg.d_model}, f={cfg.d_ff}, p0={cfg.p0}), T={T}{note}",
             "tokens_per_s": T / t, "ms_per_call": t * 1e3, "touched_experts": int(len(touched)),
             "stream_bytes": sb, "stream_gbs": sb / t / 1e9, "stream_pct_of_hbm_peak": 100.0 * sb / t / 1e9 / peak,
-            "ms_per_call_cuda_graph": t_graph * 1e3}
+            "ms_per_call_cuda_graph": t_graph * 1e3, "phase_ms": phases}
 
 
 def _rotating_dict_row(layer, cfg, T, device, peak, replicas=1, batches=1, n=60):

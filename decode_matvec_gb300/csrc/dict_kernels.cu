@@ -649,11 +649,14 @@ __global__ void __launch_bounds__(GemmBounds<DICT_SMEM, NTMAX>::threads, GemmBou
 //    256-column block of 128 rows into a dense bf16 tile of exact {-1, 0, +1}
 //    (one thread per row: its row is zeroed, then its nonzeros written); the
 //    groups take alternate blocks, so two blocks are decoded at once;
-//  * a loader warp stages the block's activations of up to 64 tokens (bf16,
-//    16-byte asynchronous copies, zero past the tokens and columns that exist);
-//  * one thread issues tcgen05.mma (M=128, N = tokens rounded up to 16, K=16,
-//    bf16 x bf16 -> fp32 in tensor memory) and commits each block to the
-//    barrier that frees its two stages;
+//  * a loader warp stages the activations of up to 256 tokens, 64 columns (an
+//    atom) at a time, into three atom stages (bf16, 16-byte asynchronous
+//    copies, zero past the tokens and columns that exist), so an expert's
+//    tiles are decoded once per 256 of its tokens;
+//  * one thread issues tcgen05.mma (M=128, N = tokens rounded up to 16, up to
+//    256, K=16, bf16 x bf16 -> fp32 in tensor memory) and commits each atom to
+//    the barrier that frees its B stage and each block to the one that frees
+//    its A stage;
 //  * 4 epilogue warps read a finished tile's accumulators (two accumulators in
 //    tensor memory alternate between tiles), apply the row scale and the
 //    activation or gate, and store.
@@ -663,16 +666,16 @@ __global__ void __launch_bounds__(GemmBounds<DICT_SMEM, NTMAX>::threads, GemmBou
 // as the CUDA-core kernel, summed in another order.  Every wait is bounded:
 // on expiry the kernel records QMOE_ETIMEOUT, waits (bounded) for its
 // outstanding MMAs, frees its tensor memory and returns.
-constexpr int kDtcM = 128, kDtcN = 64, kDtcK = 256;
+constexpr int kDtcM = 128, kDtcN = 256, kDtcK = 256;
 constexpr int kDtcStageA = kDtcM * kDtcK * 2;                 // 64 KB per A stage
-constexpr int kDtcStageB = kDtcN * kDtcK * 2;                 // 32 KB per B stage
 constexpr int kDtcAtomA = kDtcM * 128;                        // one 64-column atom of A (16 KB)
-constexpr int kDtcAtomB = kDtcN * 128;                        // ... of B (8 KB)
+constexpr int kDtcAtomB = kDtcN * 128;                        // ... of B (32 KB): one B stage
 constexpr int kDtcDecWarps = 8, kDtcEpiWarp = 8, kDtcLoadWarp = 12, kDtcMmaWarp = 13;
 constexpr int kDtcThreads = 14 * 32;
 constexpr int kDtcTmemCols = 2 * kDtcN;                       // two accumulators
-constexpr int kDtcStagesB = 3;                                 // activation stages (the loader runs ahead)
-constexpr int kDtcSmem = 1024 + 2 * kDtcStageA + kDtcStagesB * kDtcStageB + 192;
+constexpr int kDtcStagesB = 3;                                 // activation atom stages (the loader runs ahead)
+constexpr int kDtcSmem = 1024 + 2 * kDtcStageA + kDtcStagesB * kDtcAtomB + 192;
+static_assert(kDtcSmem <= kSmemMax && kDtcTmemCols <= 512, "tensor-core kernel resources");
 constexpr uint32_t kDtcSpin = 1u << 22;
 constexpr uint16_t kBf16One = 0x3F80, kBf16MinusOne = 0xBF80;
 
@@ -849,19 +852,23 @@ __device__ __forceinline__ void tc_store(const GemmArgs& a, int slot, int row, f
     }
 }
 
-// A finished tile's outputs: lane i of the warp holds the slots of tokens i and i + 32 and hands
+// A finished tile's outputs: lane i of the warp holds the slots of tokens i, i + 32, ... and hands
 // each to the whole warp when its column is stored.
 template <int MODE>
-__device__ __forceinline__ void tc_epilogue_tile(const GemmArgs& a, uint32_t taddr, int slot_lo, int slot_hi, int n_tok,
-                                                 int row, float s) {
-    for (int n0 = 0; n0 < n_tok; n0 += 8) {
-        uint32_t r[8];
-        tmem_ld8(taddr + (uint32_t)n0, r);
+__device__ __forceinline__ void tc_epilogue_tile(const GemmArgs& a, uint32_t taddr, const int (&slot)[kDtcN / 32],
+                                                 int n_tok, int row, float s) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int n = n0 + q;
-            const int slot = __shfl_sync(QMOE_FULL_MASK, n < 32 ? slot_lo : slot_hi, n & 31);
-            if (n < n_tok && row < a.m.rows) tc_store<MODE>(a, slot, row, s * __uint_as_float(r[q]));
+    for (int i = 0; i < kDtcN / 32; ++i) {
+        if (32 * i >= n_tok) break;
+        for (int n1 = 0; n1 < 32 && 32 * i + n1 < n_tok; n1 += 8) {
+            uint32_t r[8];
+            tmem_ld8(taddr + (uint32_t)(32 * i + n1), r);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int n = 32 * i + n1 + q;
+                const int sl = __shfl_sync(QMOE_FULL_MASK, slot[i], n1 + q);
+                if (n < n_tok && row < a.m.rows) tc_store<MODE>(a, sl, row, s * __uint_as_float(r[q]));
+            }
         }
     }
 }
@@ -871,7 +878,7 @@ __global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs 
     unsigned char* smem = (unsigned char*)(((uintptr_t)g_smem + 1023) & ~(uintptr_t)1023);
     unsigned char* stA = smem;                                   // 2 stages
     unsigned char* stB = smem + 2 * kDtcStageA;                  // 2 stages
-    uint64_t* bars = (uint64_t*)(stB + kDtcStagesB * kDtcStageB);
+    uint64_t* bars = (uint64_t*)(stB + kDtcStagesB * kDtcAtomB);
     uint64_t* full_a = bars;          // [2] decoders of a stage's group (4 warp arrivals)
     uint64_t* empty_a = bars + 2;     // [2] MMA commit: the A stage was read
     uint64_t* acc_full = bars + 4;    // [2] MMA commit: a tile's accumulator is final
@@ -979,8 +986,10 @@ __global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs 
             const Job job = a.jobs[tile / a.row_tiles];
             const int row = (tile % a.row_tiles) * kDtcM + 32 * ew + lane;
             const uint32_t acc = t & 1u;
-            const int slot_lo = lane < job.n_tok ? a.slots[job.slot_begin + lane] : 0;
-            const int slot_hi = lane + 32 < job.n_tok ? a.slots[job.slot_begin + lane + 32] : 0;
+            int slot[kDtcN / 32];
+#pragma unroll
+            for (int i = 0; i < kDtcN / 32; ++i)
+                slot[i] = lane + 32 * i < job.n_tok ? a.slots[job.slot_begin + lane + 32 * i] : 0;
             const float s = row < m.rows ? f16_to_f32(m.scale[(size_t)job.matrix * m.rows + row]) : 0.0f;
             if (!mbar_wait_sleep(acc_full + acc, (t >> 1) & 1u, kDtcSpin) || *abort_v) {
                 timed_out = true;
@@ -989,61 +998,65 @@ __global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs 
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(32 * ew) << 16) + acc * kDtcN;
             switch (a.mode) {
-                case OUT_RELU_H: tc_epilogue_tile<OUT_RELU_H>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
-                case OUT_GATED: tc_epilogue_tile<OUT_GATED>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
-                case OUT_SLOT_F32: tc_epilogue_tile<OUT_SLOT_F32>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
-                default: tc_epilogue_tile<OUT_PLAIN>(a, taddr, slot_lo, slot_hi, job.n_tok, row, s); break;
+                case OUT_RELU_H: tc_epilogue_tile<OUT_RELU_H>(a, taddr, slot, job.n_tok, row, s); break;
+                case OUT_GATED: tc_epilogue_tile<OUT_GATED>(a, taddr, slot, job.n_tok, row, s); break;
+                case OUT_SLOT_F32: tc_epilogue_tile<OUT_SLOT_F32>(a, taddr, slot, job.n_tok, row, s); break;
+                default: tc_epilogue_tile<OUT_PLAIN>(a, taddr, slot, job.n_tok, row, s); break;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty + acc);
         }
     } else if (warp == kDtcLoadWarp) {
-        // ---------------- loader: activations of block b into stage b % 3; a stage is announced once
-        // the copies of the next block are issued (so its own copies have had a block's time to land)
-        uint32_t gb = 0;
-        int pending = -1;                                   // block whose copies are in flight
+        // ---------------- loader: activations of atom g (64 columns of up to 256 tokens) into stage
+        // g % 3; a stage is announced once the copies of the next atom are issued (so its own copies
+        // have had an atom's time to land).  Lane l copies the rows of tokens l, l + 32, ...; rows past
+        // the tokens (up to the MMA's N) are zero-filled, rows past N are not touched.
+        uint32_t ga = 0;
+        int pending = -1;                                   // atom whose copies are in flight
         for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
             const Job job = a.jobs[tile / a.row_tiles];
-            const uint16_t* src[2];
-            uint32_t rowo[2], sw[2];
+            const int n16 = min(kDtcN, (job.n_tok + 15) & ~15);
+            const uint16_t* src[kDtcN / 32];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kDtcN / 32; ++i) {
                 const int n = lane + 32 * i;
-                src[i] = n < job.n_tok ? a.x + (size_t)(a.slots[job.slot_begin + n] / a.x_div) * m.cols : a.x;
-                rowo[i] = (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u;
-                sw[i] = (uint32_t)(n & 7);
+                src[i] = n < job.n_tok ? a.x + (size_t)(a.slots[job.slot_begin + n] / a.x_div) * m.cols : nullptr;
             }
-            const bool has[2] = {lane < job.n_tok, lane + 32 < job.n_tok};
-            for (int b = 0; b < nb; ++b, ++gb) {
-                const uint32_t s = gb % kDtcStagesB, use = gb / kDtcStagesB;
-                if (!mbar_wait_sleep(empty_b + s, (use & 1u) ^ 1u, kDtcSpin) || *abort_v) {
-                    timed_out = true;
-                    break;
-                }
-                const uint32_t B = smem_u32(stB + s * kDtcStageB);
-                const int c0 = b * kDtcK;
-                const int live_ch = min(kDtcK, m.cols - c0) / 8;     // whole 16-byte chunks of the block
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const uint16_t* p = src[i] + c0;
-#pragma unroll 8
-                    for (int ch = 0; ch < kDtcK / 8; ++ch) {
-                        const bool live = has[i] && ch < live_ch;
-                        const uint32_t dst = B + (uint32_t)(ch >> 3) * kDtcAtomB + rowo[i] + (((uint32_t)ch ^ sw[i]) & 7u) * 16u;
-                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
-                                     "l"(live ? p + ch * 8 : a.x), "r"(live ? 16 : 0)
-                                     : "memory");
+            const uint32_t rowo = (uint32_t)(lane >> 3) * 1024u + (uint32_t)(lane & 7) * 128u, sw = (uint32_t)(lane & 7);
+            for (int b = 0; b < nb && !timed_out; ++b) {
+                const int kcols = min(kDtcK, m.cols - b * kDtcK);
+                for (int at = 0; at < (kcols + 63) / 64; ++at, ++ga) {
+                    const uint32_t s = ga % kDtcStagesB, use = ga / kDtcStagesB;
+                    if (!mbar_wait_sleep(empty_b + s, (use & 1u) ^ 1u, kDtcSpin) || *abort_v) {
+                        timed_out = true;
+                        break;
                     }
+                    const uint32_t B = smem_u32(stB + s * kDtcAtomB);
+                    const int c0 = b * kDtcK + 64 * at;
+                    const int live_ch = min(64, m.cols - c0) / 8;     // whole 16-byte chunks of the atom
+#pragma unroll
+                    for (int i = 0; i < kDtcN / 32; ++i) {
+                        if (32 * i >= n16) break;
+                        const uint16_t* p = src[i] ? src[i] + c0 : a.x;
+                        const uint32_t rb = B + (uint32_t)(4 * i) * 1024u + rowo;   // token lane + 32 i
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const bool live = src[i] && ch < live_ch;
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(rb + ((((uint32_t)ch ^ sw) & 7u) << 4)),
+                                         "l"(live ? p + ch * 8 : a.x), "r"(live ? 16 : 0)
+                                         : "memory");
+                        }
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    if (pending >= 0) {
+                        asm volatile("cp.async.wait_group 1;" ::: "memory");
+                        fence_async_shared();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(full_b + (uint32_t)pending % kDtcStagesB);
+                    }
+                    pending = (int)ga;
                 }
-                asm volatile("cp.async.commit_group;" ::: "memory");
-                if (pending >= 0) {
-                    asm volatile("cp.async.wait_group 1;" ::: "memory");
-                    fence_async_shared();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(full_b + (uint32_t)pending % kDtcStagesB);
-                }
-                pending = (int)gb;
             }
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -1052,9 +1065,9 @@ __global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs 
             __syncwarp();
             if (lane == 0) mbar_arrive(full_b + (uint32_t)pending % kDtcStagesB);
         }
-    } else if (lane == 0) {
+    } else if (warp == kDtcMmaWarp && lane == 0) {
         // ---------------- MMA issuer
-        uint32_t gb = 0, t = 0;
+        uint32_t gb = 0, ga = 0, t = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x, ++t) {
             const Job job = a.jobs[tile / a.row_tiles];
             const uint32_t acc = t & 1u;
@@ -1065,32 +1078,40 @@ __global__ void __launch_bounds__(kDtcThreads, 1) dict_tc_kernel(const GemmArgs 
             tc_fence_after();
             const int n16 = min(kDtcN, (job.n_tok + 15) & ~15);
             const uint32_t idesc = idesc_f16(kDtcM, n16, true, true);
-            for (int b = 0; b < nb; ++b, ++gb) {
-                const uint32_t s = gb & 1u, sb = gb % kDtcStagesB;
-                if (!mbar_wait_sleep(full_a + s, (gb >> 1) & 1u, kDtcSpin) ||
-                    !mbar_wait_sleep(full_b + sb, (gb / kDtcStagesB) & 1u, kDtcSpin) || *abort_v) {
+            for (int b = 0; b < nb && !timed_out; ++b, ++gb) {
+                const uint32_t s = gb & 1u;
+                if (!mbar_wait_sleep(full_a + s, (gb >> 1) & 1u, kDtcSpin) || *abort_v) {
                     timed_out = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(stA + s * kDtcStageA), b0 = smem_u32(stB + sb * kDtcStageB);
-                const int ksteps = (min(kDtcK, m.cols - b * kDtcK) + 15) / 16;
-                for (int k = 0; k < ksteps; ++k) {
-                    const uint32_t ko = (uint32_t)(k & 3) * 32u;
-                    mma_f16(tmem + acc * kDtcN, umma_desc_sw128(a0 + (uint32_t)(k >> 2) * kDtcAtomA + ko),
-                            umma_desc_sw128(b0 + (uint32_t)(k >> 2) * kDtcAtomB + ko), idesc, b > 0 || k > 0);
+                const uint32_t a0 = smem_u32(stA + s * kDtcStageA);
+                const int kcols = min(kDtcK, m.cols - b * kDtcK);
+                for (int at = 0; at < (kcols + 63) / 64; ++at, ++ga) {
+                    const uint32_t sb = ga % kDtcStagesB;
+                    if (!mbar_wait_sleep(full_b + sb, (ga / kDtcStagesB) & 1u, kDtcSpin) || *abort_v) {
+                        timed_out = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b0 = smem_u32(stB + sb * kDtcAtomB);
+                    const int ksteps = min(4, (kcols - 64 * at + 15) / 16);
+                    for (int k = 0; k < ksteps; ++k)
+                        mma_f16(tmem + acc * kDtcN, umma_desc_sw128(a0 + (uint32_t)at * kDtcAtomA + (uint32_t)k * 32u),
+                                umma_desc_sw128(b0 + (uint32_t)k * 32u), idesc, b > 0 || at > 0 || k > 0);
+                    mma_commit(empty_b + sb);
                 }
+                if (timed_out) break;
                 mma_commit(empty_a + s);
-                mma_commit(empty_b + sb);
             }
             if (timed_out) break;
             mma_commit(acc_full + acc);
         }
         if (timed_out) {
             *abort_v = 1;
-            // the tensor core may still be working on committed blocks: wait (bounded) for the last
-            // commit before the memory is released
-            if (gb > 0) mbar_wait_sleep(empty_a + ((gb - 1) & 1u), ((gb - 1) >> 1) & 1u, kDtcSpin);
+            // the tensor core may still be working on committed atoms: wait (bounded) for the commit
+            // of the last one (it follows every earlier MMA) before the memory is released
+            if (ga > 0) mbar_wait_sleep(empty_b + (ga - 1) % kDtcStagesB, ((ga - 1) / kDtcStagesB) & 1u, kDtcSpin);
         }
     }
     if (timed_out) *abort_v = 1;
