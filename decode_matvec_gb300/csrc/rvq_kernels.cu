@@ -601,7 +601,13 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq_gemm_kernel(const RvqGemmA
 }
 
 // ---------------------------------------------------------------- decode-multiply (tcgen05 tensor cores)
-// For T >= 16 the RVQ product is a real dense contraction per expert: a CTA
+// E8P sets: rvq_tc_kernel below.  Codebook (RVQ) sets: rvq_ws_kernel further
+// down, a warp-specialised form that is faster where a K chunk takes several
+// decode steps (one per residual stage); with E8P's single step per chunk the
+// per-step handoff of its ring costs more than it hides (OLMoE-shaped layer at
+// T = 32: E8P 0.27 ms here, 0.30 ms there; 2-stage RVQ 0.42 ms here, 0.38 there).
+//
+// For T >= 16 the product is a real dense contraction per expert: a CTA
 // takes 128 output rows of one expert matrix and up to 32 of its tokens.  For
 // every 128-wide K chunk, 256 threads decode the 128 x 128 weight tile
 // (C1[i1] + C2[i2] in fp32, rounded to fp16) and the 32 x 128 activation tile
@@ -918,7 +924,10 @@ __global__ void __launch_bounds__(kTcThreads) rvq_tc_kernel(const RvqGemmArgs a)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcNM) : "memory");
 }
 
+int launch_rvq_ws(RvqGemmArgs a, cudaStream_t st, long long tiles_hint);
+
 int launch_rvq_tc(RvqGemmArgs a, cudaStream_t st, long long tiles_hint) {
+    if (!a.m.e8p) return launch_rvq_ws(a, st, tiles_hint);
     int rc = qmoe::smem_attr((const void*)rvq_tc_kernel, kTcSmem, "rvq tc attr");
     if (rc) return rc;
     a.rows_per_tile = kTcM;
@@ -926,6 +935,426 @@ int launch_rvq_tc(RvqGemmArgs a, cudaStream_t st, long long tiles_hint) {
     const long long grid = std::max(1LL, std::min(tiles_hint, (long long)qmoe::sm_count() * 2));
     rvq_tc_kernel<<<(unsigned)grid, kTcThreads, kTcSmem, st>>>(a);
     return qmoe::launch_check("rvq_tc_kernel");
+}
+
+// ---------------------------------------------------------------- decode-multiply, warp-specialised (codebook sets)
+// A tile is 128 output rows of one expert matrix and up to 32 of its tokens.
+// One persistent CTA per SM, warp-specialised:
+//  * 16 producer warps decode, for every 128-wide K chunk and every residual
+//    stage (a "step"), the stage's exact fp16 codewords of the tile's rows into
+//    a weight tile of a ring of three, in the canonical no-swizzle K-major
+//    layout (8-row x 16-byte core matrices; neighbours along K 128 B apart,
+//    along M/N 2048 B apart), and at a chunk's first step the chunk's rotated
+//    activations as fp16 high parts and fp16 remainders (one N=64 operand,
+//    two chunk buffers alternate).  The codebooks sit in shared memory eight
+//    times, replica j holding every entry in 16-byte bank group j, and the
+//    eight lanes of a quarter-warp read replicas 0..7: the gathers are free of
+//    bank conflicts, as are the tile stores (a quarter-warp fills one core
+//    matrix);
+//  * one thread issues the step's eight tcgen05.mma (M=128, N=64, K=16, fp16 x
+//    fp16 -> fp32 in tensor memory) once the step's barrier completes, and
+//    commits them to the barriers that free the weight tile and, after the
+//    chunk's last step, its activations;
+//  * 4 epilogue warps read a finished tile's accumulator (two alternate, so the
+//    next tile's MMAs run meanwhile), add the high and low parts' columns,
+//    undo the staging scale, apply the row scale and store.
+// Every wait is bounded: on expiry the kernel records
+// QMOE_ETIMEOUT, waits (bounded) for its outstanding MMAs, frees its tensor
+// memory and returns.
+
+constexpr int kWsM = 128, kWsN = 32, kWsK = 128;
+constexpr int kWsProd = 512;                               // producer threads (16 warps)
+constexpr int kWsMmaWarp = kWsProd / 32;                   // then 4 epilogue warps
+constexpr int kWsThreads = kWsProd + 5 * 32;
+constexpr int kWsVpt = kWsM * (kWsK / 8) / kWsProd;        // 8-weight vectors each producer decodes per step (4)
+constexpr int kWsBpt = kWsN * kWsK / kWsProd;              // activations each producer stages per chunk (8)
+static_assert(kWsVpt == 4 && kWsBpt == 8, "thread mapping of rvq_ws_kernel");
+constexpr int kWsLBO = 128;                       // core matrices adjacent along K
+constexpr int kWsSBO = (kWsK / 8) * 128;          // core matrices adjacent along M / N (2048 B)
+constexpr int kWsABytes = kWsM * kWsK * 2;        // 32 KB
+constexpr int kWsBBytes = kWsN * kWsK * 2;        // 8 KB (high parts; the low parts follow)
+constexpr int kWsRing = 3;                        // weight tiles
+constexpr int kWsCbRep = 8;                       // codebook replicas (one per 16-byte bank group)
+constexpr int kWsCbBytes = QMOE_RVQ_MAX_STAGES * 256 * kWsCbRep * 16;
+constexpr int kWsBarBytes = 128;
+constexpr int kWsSmem = 1024 /*align*/ + kWsCbBytes + kWsRing * kWsABytes + 4 * kWsBBytes + kWsBarBytes;
+static_assert(kWsSmem <= 232448, "rvq_ws_kernel shared memory");
+constexpr uint32_t kWsSpinLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t ws_smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t ws_umma_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(kWsLBO >> 4) << 16;
+    d |= (uint64_t)(kWsSBO >> 4) << 32;
+    d |= 1ull << 46;                              // descriptor version for tcgen05
+    return d;                                     // base offset 0, swizzle none
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major, N = 64, M = 128.
+// MMA N = 2 * kWsN: the activations' fp16 high parts are B rows 0..31, their low parts rows 32..63
+constexpr int kWsNM = 2 * kWsN;
+constexpr uint32_t kWsIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kWsNM >> 3) << 17) |
+                              ((uint32_t)(kWsM >> 4) << 24);
+constexpr int kWsTmemCols = 2 * kWsNM;            // two accumulators
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(ws_smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ws_smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_to(uint64_t* b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(ws_smem_u32(b))
+                 : "memory");
+}
+
+// Bounded wait for the phase of the given parity (suspending between tries); false when the bound ran out.
+__device__ __forceinline__ bool ws_mbar_wait(uint64_t* b, uint32_t parity) {
+    const uint32_t bar = ws_smem_u32(b);
+    for (uint32_t it = 0; it < kWsSpinLimit; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(1000u)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// 16 consecutive fp32 accumulator columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16_at(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Codebooks [n_st][256] x 16 bytes into shared memory, entry e of stage s in
+// all replicas: replica j at 16-byte slot j of the 128-byte line (s * 256 + e).
+// Run by the 256 producer threads (thread i loads entry i of every stage).
+__device__ __forceinline__ void rvq_stage_codebooks_rep(const uint4* __restrict__ g, uint4* t, int n_st, int tid) {
+    uint4 c[QMOE_RVQ_MAX_STAGES];
+#pragma unroll
+    for (int s = 0; s < QMOE_RVQ_MAX_STAGES; ++s) c[s] = s < n_st ? __ldg(g + tid + s * 256) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int s = 0; s < QMOE_RVQ_MAX_STAGES; ++s) {
+        if (s < n_st) {
+#pragma unroll
+            for (int j = 0; j < kWsCbRep; ++j) t[(s * 256 + tid) * kWsCbRep + j] = c[s];
+        }
+    }
+}
+
+// Copies a thread's kWsVpt consecutive stage-`st` codewords (exact fp16 rows
+// of codebook st, from replica j; the vectors' S code bytes each are in the S
+// words of cw) to consecutive core matrices along K of its weight-tile row.
+__device__ __forceinline__ void ws_stage_run(const uint4* scb, const uint32_t (&cw)[QMOE_RVQ_MAX_STAGES], int S, int st,
+                                          int j, unsigned char* dst) {
+#pragma unroll
+    for (int q = 0; q < kWsVpt; ++q) {
+        const int byte = q * S + st;                      // < 4 * QMOE_RVQ_MAX_STAGES
+        const uint32_t w = byte < 4 ? cw[0] : byte < 8 ? cw[1] : cw[2];
+        const uint32_t code = (w >> (8 * (byte & 3))) & 255u;
+        *(uint4*)(dst + q * kWsLBO) = scb[(256 * st + code) * kWsCbRep + j];
+    }
+}
+
+// The job of tile `tile` and its first row.
+__device__ __forceinline__ Job rvq_tile_job(const RvqGemmArgs& a, int tile, int& r0) {
+    Job job;
+    const int j = tile / a.row_tiles;
+    if (a.jobs) {
+        job = a.jobs[j];
+    } else {
+        job.matrix = 0;
+        job.slot_begin = j * kWsN;
+        job.n_tok = min(kWsN, a.T_implicit - j * kWsN);
+    }
+    r0 = (tile % a.row_tiles) * kWsM;
+    return job;
+}
+
+// Warms L2 with the code bytes of tile `tile` (its rows are contiguous: 128 rows x cols/8 x S
+// bytes), rounded inwards to 16-byte boundaries.
+__device__ void rvq_prefetch_tile(const RvqGemmArgs& a, int tile, int n_tiles) {
+    if (tile >= n_tiles) return;
+    int r0;
+    const Job job = rvq_tile_job(a, tile, r0);
+    const RvqDev& m = a.m;
+    if (m.stages && (m.stages[job.matrix] < 1 || m.stages[job.matrix] > m.n_st)) return;
+    const int S = m.stages ? m.stages[job.matrix] : 2;
+    const size_t row_bytes = (size_t)(m.cols / 8) * S;
+    const int r1 = min(m.rows, r0 + kWsM);
+    const uintptr_t lo = ((uintptr_t)(codes_of(m, job.matrix) + (size_t)r0 * row_bytes) + 15) & ~(uintptr_t)15;
+    const uintptr_t hi = (uintptr_t)(codes_of(m, job.matrix) + (size_t)r1 * row_bytes) & ~(uintptr_t)15;
+    for (uintptr_t p = lo; p < hi;) {
+        const uint32_t n = (uint32_t)min((uintptr_t)(1u << 20), hi - p);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+        p += n;
+    }
+}
+
+__global__ void __launch_bounds__(kWsThreads, 1) rvq_ws_kernel(const RvqGemmArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint4* scb = (uint4*)smem;
+    uint8_t* ring = smem + kWsCbBytes;                            // kWsRing weight tiles
+    uint8_t* bbuf = ring + kWsRing * kWsABytes;                   // 2 chunks x (high, low)
+    uint64_t* bars = (uint64_t*)(bbuf + 4 * kWsBBytes);
+    uint64_t* a_full = bars;                     // [kWsRing] producers (one arrival per warp)
+    uint64_t* a_empty = bars + kWsRing;          // [kWsRing] MMA commit: the weight tile was read
+    uint64_t* b_full = bars + 2 * kWsRing;       // [2] producers (one arrival per warp)
+    uint64_t* b_empty = b_full + 2;              // [2] MMA commit after the chunk's last step
+    uint64_t* acc_full = b_full + 4;             // [2] MMA commit: the tile's accumulator is final
+    uint64_t* acc_empty = b_full + 6;            // [2] epilogue warps (4 arrivals)
+    uint32_t* tmem_slot = (uint32_t*)(b_full + 8);
+    int* abort_flag = (int*)(tmem_slot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const RvqDev& m = a.m;
+
+    if (tid < 256) rvq_stage_codebooks_rep((const uint4*)m.cb, scb, m.n_st, tid);
+    if (tid == 0) {
+        for (int s = 0; s < kWsRing; ++s) {
+            bar_init(a_full + s, kWsProd / 32);
+            bar_init(a_empty + s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            bar_init(b_full + s, kWsProd / 32);
+            bar_init(b_empty + s, 1);
+            bar_init(acc_full + s, 1);
+            bar_init(acc_empty + s, 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(ws_smem_u32(tmem_slot)),
+                     "r"(kWsTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+    volatile int* abort_v = abort_flag;
+
+    bool timed_out = false;
+    const int nv = m.cols / 8;
+    const int nk = m.cols / kWsK;
+    const int n_jobs = a.jobs ? *a.n_jobs_dev : (a.T_implicit + kWsN - 1) / kWsN;
+    const int n_tiles = n_jobs * a.row_tiles;
+
+    if (warp < kWsProd / 32) {
+        // ---------------- producers: weight tiles of every step, activations of every chunk
+        // per thread: A part (row, a quarter of a chunk's 16 vectors), B part (token, one 8-wide K
+        // group); the 8 lanes of a quarter-warp take 8 consecutive rows (tokens), so their 16-byte tile
+        // stores fill one 128-byte core matrix, and read codebook replicas 0..7
+        const int rl = (tid & 7) | ((tid >> 5) << 3), part = (tid >> 3) & 3, rep = tid & 7;
+        const int bn = (tid & 7) | ((tid >> 7) << 3), bg = (tid >> 3) & 15;
+        uint32_t gs = 0, gc = 0;
+        if (tid == 0) rvq_prefetch_tile(a, blockIdx.x, n_tiles);
+        for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+            // the next tile's codes travel towards L2 while this one is decoded
+            if (tid == 0) rvq_prefetch_tile(a, tile + gridDim.x, n_tiles);
+            int r0;
+            const Job job = rvq_tile_job(a, tile, r0);
+            const int S = stages_of(m, job.matrix);          // code bytes per vector
+            if (S == 0) continue;                             // every role skips the tile
+            const int arow = r0 + rl;
+            const uint8_t* ip = codes_of(m, job.matrix) + ((size_t)(arow < m.rows ? arow : 0) * nv + part * kWsVpt) * S;
+            const int bslot = bn < job.n_tok ? (a.slots ? a.slots[job.slot_begin + bn] : job.slot_begin + bn) : -1;
+            const float* bp = a.xr + (size_t)(bslot < 0 ? 0 : bslot) * m.cols + bg * 8;
+            // the token's staging scale: a power of two, applied before the fp16 split and undone in
+            // the epilogue (exact)
+            const float bscale = bslot >= 0 && a.xs ? __ldg(a.xs + bslot) : 1.0f;
+            // the global loads of chunk kc + 1 are issued before chunk kc is decoded; a thread's
+            // kWsVpt vectors of a chunk are 4 * S code bytes, as S 4-byte loads
+            uint32_t cw_n[QMOE_RVQ_MAX_STAGES];
+#pragma unroll
+            for (int q = 0; q < QMOE_RVQ_MAX_STAGES; ++q)
+                cw_n[q] = arow < m.rows && q < S ? __ldg((const uint32_t*)ip + q) : 0u;
+            float4 xv_n[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                xv_n[q] = bslot >= 0 ? __ldg((const float4*)bp + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int n_steps = S;
+            for (int kc = 0; kc < nk && !timed_out; ++kc, ++gc) {
+                uint32_t cw[QMOE_RVQ_MAX_STAGES];
+#pragma unroll
+                for (int q = 0; q < QMOE_RVQ_MAX_STAGES; ++q) cw[q] = cw_n[q];
+                float4 xv[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) xv[q] = xv_n[q];
+                if (kc + 1 < nk) {
+                    if (arow < m.rows) {
+                        const uint32_t* nx = (const uint32_t*)(ip + (size_t)(kc + 1) * (kWsK / 8) * S);
+#pragma unroll
+                        for (int q = 0; q < QMOE_RVQ_MAX_STAGES; ++q)
+                            if (q < S) cw_n[q] = __ldg(nx + q);
+                    }
+                    if (bslot >= 0) {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) xv_n[q] = __ldg((const float4*)(bp + (size_t)(kc + 1) * kWsK) + q);
+                    }
+                }
+                uint8_t* Bh = bbuf + (gc & 1u) * 2 * kWsBBytes;        // N = 64 rows: high parts, then low
+                uint8_t* Bl = Bh + 4 * kWsSBO;
+                for (int st = 0; st < n_steps; ++st, ++gs) {
+                    const uint32_t slot = gs % kWsRing;
+                    bool ok = ws_mbar_wait(a_empty + slot, ((gs / kWsRing) & 1u) ^ 1u);
+                    if (st == 0) ok = ok && ws_mbar_wait(b_empty + (gc & 1u), ((gc >> 1) & 1u) ^ 1u);
+                    ok = ok && !*abort_v;
+                    if (__any_sync(QMOE_FULL_MASK, !ok)) {
+                        timed_out = true;
+                        break;
+                    }
+                    uint8_t* A = ring + slot * kWsABytes;
+                    unsigned char* arow_base = A + (rl >> 3) * kWsSBO + (rl & 7) * 16 + part * kWsVpt * kWsLBO;
+                    if (arow >= m.rows) {
+#pragma unroll
+                        for (int q = 0; q < kWsVpt; ++q) *(uint4*)(arow_base + q * kWsLBO) = make_uint4(0, 0, 0, 0);
+                    } else {
+                        ws_stage_run(scb, cw, S, st, rep, arow_base);
+                    }
+                    if (st == 0) {
+                        const float v[8] = {xv[0].x * bscale, xv[0].y * bscale, xv[0].z * bscale, xv[0].w * bscale,
+                                            xv[1].x * bscale, xv[1].y * bscale, xv[1].z * bscale, xv[1].w * bscale};
+                        const int o = (bn >> 3) * kWsSBO + bg * kWsLBO + (bn & 7) * 16;
+                        store_hi_lo8(Bh + o, Bl + o, v);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        bar_arrive(a_full + slot);
+                        if (st == 0) bar_arrive(b_full + (gc & 1u));
+                    }
+                }
+            }
+        }
+    } else if (warp == kWsMmaWarp) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            uint32_t gs = 0, gc = 0, t = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+                int r0;
+                const Job job = rvq_tile_job(a, tile, r0);
+                const int S = stages_of(m, job.matrix);
+                if (S == 0) continue;
+                const uint32_t acc = t & 1u;
+                if (!ws_mbar_wait(acc_empty + acc, ((t >> 1) & 1u) ^ 1u) || *abort_v) {
+                    timed_out = true;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t d = tmem + acc * (uint32_t)kWsNM;
+                const int n_steps = S;
+                for (int kc = 0; kc < nk && !timed_out; ++kc, ++gc) {
+                    const uint32_t b0 = ws_smem_u32(bbuf + (gc & 1u) * 2 * kWsBBytes);
+                    for (int st = 0; st < n_steps; ++st) {
+                        const uint32_t slot = gs % kWsRing;
+                        bool ok = ws_mbar_wait(a_full + slot, (gs / kWsRing) & 1u);
+                        if (st == 0) ok = ok && ws_mbar_wait(b_full + (gc & 1u), (gc >> 1) & 1u);
+                        if (!ok || *abort_v) {
+                            timed_out = true;
+                            break;
+                        }
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        const uint32_t a0 = ws_smem_u32(ring + slot * kWsABytes);
+#pragma unroll
+                        for (int k = 0; k < kWsK / 16; ++k) {
+                            const uint32_t accf = (kc > 0 || st > 0 || k > 0) ? 1u : 0u;
+                            asm volatile(
+                                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+                                "l"(ws_umma_desc(a0 + k * 2 * kWsLBO)), "l"(ws_umma_desc(b0 + k * 2 * kWsLBO)), "r"(kWsIdesc),
+                                "r"(accf)
+                                : "memory");
+                        }
+                        mma_commit_to(a_empty + slot);
+                        if (st == n_steps - 1) mma_commit_to(b_empty + (gc & 1u));
+                        ++gs;
+                    }
+                }
+                if (timed_out) break;
+                mma_commit_to(acc_full + acc);
+                ++t;
+            }
+            if (timed_out) {
+                *abort_v = 1;
+                // the tensor core may still be working on committed steps: wait (bounded) for the
+                // last one before the memory is released
+                if (gs > 0) ws_mbar_wait(a_empty + (gs - 1) % kWsRing, ((gs - 1) / kWsRing) & 1u);
+            }
+        }
+    } else {
+        // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+        const int qw = warp & 3;
+        uint32_t t = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !timed_out; tile += gridDim.x) {
+            int r0;
+            const Job job = rvq_tile_job(a, tile, r0);
+            const int S = stages_of(m, job.matrix);
+            if (S == 0) continue;
+            const uint32_t acc = t & 1u;
+            // lane n holds token n's slot and the inverse of its staging scale (exact: a power of
+            // two); they and the row scale are read while the tile's MMAs run
+            const int row = r0 + 32 * qw + lane;
+            const int my_slot = lane < job.n_tok ? (a.slots ? a.slots[job.slot_begin + lane] : job.slot_begin + lane) : 0;
+            const float my_inv = lane < job.n_tok && a.xs ? 1.0f / __ldg(a.xs + my_slot) : 1.0f;
+            const float s = row < m.rows ? f16_to_f32(m.scale[(size_t)job.matrix * m.rows + row]) : 0.0f;
+            const bool ok = ws_mbar_wait(acc_full + acc, (t >> 1) & 1u) && !*abort_v;
+            if (__any_sync(QMOE_FULL_MASK, !ok)) {
+                timed_out = true;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+
+            const uint32_t taddr = tmem + ((uint32_t)(32 * qw) << 16) + acc * (uint32_t)kWsNM;
+#pragma unroll
+            for (int h = 0; h < kWsN / 16; ++h) {
+                uint32_t r[16], rl2[16];
+                tmem_ld16_at(taddr + 16 * h, r);                    // the high parts' columns
+                tmem_ld16_at(taddr + kWsN + 16 * h, rl2);           // the low parts' columns
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int n = 16 * h + q;
+                    const int slot = __shfl_sync(QMOE_FULL_MASK, my_slot, n);
+                    const float inv = __shfl_sync(QMOE_FULL_MASK, my_inv, n);
+                    if (n < job.n_tok && row < m.rows)
+                        a.out[(size_t)slot * m.rows + row] = s * ((__uint_as_float(r[q]) + __uint_as_float(rl2[q])) * inv);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) bar_arrive(acc_empty + acc);
+            ++t;
+        }
+    }
+    if (timed_out) *abort_v = 1;
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (tid == 0 && *abort_v) atomicCAS(&g_rvq_error, 0, QMOE_ETIMEOUT);
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kWsTmemCols) : "memory");
+}
+
+int launch_rvq_ws(RvqGemmArgs a, cudaStream_t st, long long tiles_hint) {
+    int rc = qmoe::smem_attr((const void*)rvq_ws_kernel, kWsSmem, "rvq tc attr");
+    if (rc) return rc;
+    a.rows_per_tile = kWsM;
+    a.row_tiles = (a.m.rows + kWsM - 1) / kWsM;
+    const long long grid = std::max(1LL, std::min(tiles_hint, (long long)qmoe::sm_count()));
+    rvq_ws_kernel<<<(unsigned)grid, kWsThreads, kWsSmem, st>>>(a);
+    return qmoe::launch_check("rvq_ws_kernel");
 }
 
 // ---------------------------------------------------------------- decode (test)
