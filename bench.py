@@ -1037,21 +1037,28 @@ def main():
     # experts with >= 32 tokens run on the tensor-core kernel (large launches only)
     hot = counts >= TC_MIN_TOKENS if T_MAIN >= TC_MIN_SLOTS else np.zeros(CFG.E, bool)
     kern = {}
-    for name, sel, secs_k in (("dict_gemm_kernel", (counts > 0) & ~hot, phases["wi"] + phases["wo"]),
-                              ("dict_tc_kernel", hot, phases["wi_tc"] + phases["wo_tc"])):
-        ex = np.nonzero(sel)[0]
-        n_tok = int(counts[ex].sum())
-        act = n_tok * (2 * CFG.d_model * 2 + 2 * CFG.d_ff * 2)     # x in, h out, h in, y out
-        b = layer.stream_bytes(ex) + act + (2 * 3 * 65536 if name == "dict_gemm_kernel" else 0)
-        kern[name] = {"experts": int(len(ex)), "tokens": n_tok, "launches_per_step": 2,
-                      "ms_per_step": secs_k * 1e3, "algorithmic_bytes_per_step": int(b),
-                      "achieved_gbs": (b / secs_k / 1e9) if secs_k > 0 else None}
-        if name == "dict_gemm_kernel":
-            # the CUDA-core kernel reads only the row starts, not the block lengths
-            unread = sum(layer.wi_host.expert_offset_bytes_unread_by_cuda_cores(int(e)) +
-                         layer.wo_host.expert_offset_bytes_unread_by_cuda_cores(int(e)) for e in ex)
-            kern[name]["bytes_read_per_step"] = int(b - unread)
-            kern[name]["achieved_gbs_on_bytes_read"] = (b - unread) / secs_k / 1e9 if secs_k > 0 else None
+    # the CUDA-core launches, one per matrix (which kernel each takes: the library's own choice)
+    import decode_matvec_gb300 as Q
+    wi_k, wo_k, _ = Q.qmoe_moe_layer_kernels(CFG.E, CFG.d_model, CFG.d_ff, T_MAIN, 1)
+    ex = np.nonzero((counts > 0) & ~hot)[0]
+    n_tok = int(counts[ex].sum())
+    for label, host, k_id, secs_k in (("wi", layer.wi_host, wi_k, phases["wi"]), ("wo", layer.wo_host, wo_k, phases["wo"])):
+        act = n_tok * (CFG.d_model * 2 + CFG.d_ff * 2)            # wi: x in, h out; wo: h in, y out
+        b = sum(host.expert_bytes(int(e)) for e in ex) + act + 3 * 65536
+        # the CUDA-core kernels read only the row starts, not the block lengths
+        unread = sum(host.expert_offset_bytes_unread_by_cuda_cores(int(e)) for e in ex)
+        kern[f"{Q.KERNEL_NAMES[k_id]} ({label})"] = {
+            "experts": int(len(ex)), "tokens": n_tok, "launches_per_step": 1, "ms_per_step": secs_k * 1e3,
+            "algorithmic_bytes_per_step": int(b), "achieved_gbs": (b / secs_k / 1e9) if secs_k > 0 else None,
+            "bytes_read_per_step": int(b - unread),
+            "achieved_gbs_on_bytes_read": (b - unread) / secs_k / 1e9 if secs_k > 0 else None}
+    ex = np.nonzero(hot)[0]
+    n_tok = int(counts[ex].sum())
+    secs_k = phases["wi_tc"] + phases["wo_tc"]
+    b = layer.stream_bytes(ex) + n_tok * (2 * CFG.d_model * 2 + 2 * CFG.d_ff * 2)
+    kern["dict_tc_kernel (wi, wo)"] = {"experts": int(len(ex)), "tokens": n_tok, "launches_per_step": 2,
+                                       "ms_per_step": secs_k * 1e3, "algorithmic_bytes_per_step": int(b),
+                                       "achieved_gbs": (b / secs_k / 1e9) if secs_k > 0 else None}
     dom = max(kern, key=lambda k: kern[k]["ms_per_step"])
     peak, peak_kind = hbm_peak()
     achieved = kern[dom]["achieved_gbs"]

@@ -35,6 +35,7 @@ EXPORTED = [
     "qmoe_last_error", "qmoe_decode_dense", "rvq_decode_dense", "qmoe_set_phase_events",
     "qmoe_moe_layer_noalloc", "qmoe_pack_device_ws_size", "qmoe_pack_device", "rvq_pack_stages",
     "rvq_stage_allocation", "e8p_base_table", "e8p_pack", "e8p_nearest", "qmoe_offsets_compact",
+    "qmoe_moe_layer_kernels",
 ]
 
 
@@ -78,6 +79,7 @@ _sig = {
     "qmoe_route": [_vp, _i, _i, _i, _vp, _vp, _vp],
     "qmoe_bucketise": [_vp, _i, _i, _i, _vp, _vp, _vp, _vp],
     "qmoe_moe_layer_ws_size": [_i, _i, _i, _i, _i, _vp],
+    "qmoe_moe_layer_kernels": [_i, _i, _i, _i, _i, _vp, _vp, _vp],
     "qmoe_moe_layer": [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _i, _vp, _sz, _vp],
     "rvq_expert_matmul_ws_size": [_i, _i, _i, _vp],
     "rvq_expert_matmul": [_vp, _vp, _i, _vp, _i, _vp, _sz, _vp],
@@ -400,6 +402,19 @@ def qmoe_moe_layer_ws_size(E, d_model, d_ff, T, k) -> int:
     n = ctypes.c_size_t(0)
     _check(_lib.qmoe_moe_layer_ws_size(E, d_model, d_ff, T, k, ctypes.byref(n)), "qmoe_moe_layer_ws_size")
     return n.value
+
+
+QMOE_KERNEL_FLAT, QMOE_KERNEL_ROWS, QMOE_KERNEL_FLAT_L2 = 0, 1, 2
+KERNEL_NAMES = {QMOE_KERNEL_FLAT: "dict_gemm_kernel", QMOE_KERNEL_ROWS: "dict_rows_kernel",
+                QMOE_KERNEL_FLAT_L2: "dict_gemm_kernel"}
+
+
+def qmoe_moe_layer_kernels(E, d_model, d_ff, T, k):
+    """(wi kernel, wo kernel, tensor-core launch) of a qmoe_moe_layer call with these shapes."""
+    wi, wo, tc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.qmoe_moe_layer_kernels(E, d_model, d_ff, T, k, ctypes.byref(wi), ctypes.byref(wo), ctypes.byref(tc)),
+           "qmoe_moe_layer_kernels")
+    return wi.value, wo.value, bool(tc.value)
 
 
 def qmoe_moe_layer(d: Dictionary, wi: MatrixSet, wo: MatrixSet, x, ids, gates, y, workspace, y_is_f32=True,

@@ -1765,6 +1765,12 @@ double row_round_efficiency(int rows, int nt_max) {
     return (double)groups / (double)(rounds * max_w);
 }
 
+// Launches with the compact table in shared memory take the row-per-lane kernel when a job's rows
+// fill the block's warps in nearly whole rounds (>= 95 % busy), else the flat-stream kernel, which
+// spreads a job's codewords evenly over its warps.  Measured on GB300: c2048 wi (6144 rows, 96 %)
+// 2.61 -> 2.21 ms on the row kernel, c2048 wo (2080 rows, 90 %) 2.29 ms flat against 2.43 ms.
+bool use_row_kernel(int rows, int nt_max) { return row_round_efficiency(rows, nt_max) >= 0.95; }
+
 // The row-per-lane kernel (compact table in shared memory): a tile is one 32-row group per warp of
 // the block, so a warp done with its group moves on to the next tile of the same job at once.
 int launch_rows(GemmArgs a, int nt_max, cudaStream_t st) {
@@ -1800,13 +1806,9 @@ int launch_gemm_as(const GemmArgs& a, unsigned grid, int threads, size_t smem, c
     return QMOE_OK;
 }
 
-// Launches with the compact table in shared memory take the row-per-lane kernel when a job's rows
-// fill the block's warps in nearly whole rounds (>= 95 % busy), else the flat-stream kernel, which
-// spreads a job's codewords evenly over its warps.  Measured on GB300: c2048 wi (6144 rows, 96 %)
-// 2.61 -> 2.21 ms on the row kernel, c2048 wo (2080 rows, 90 %) 2.29 ms flat against 2.43 ms.
 int launch_gemm(GemmArgs a, bool dict_smem, int nt_max, int rows_per_tile, cudaStream_t st, long long tiles_hint) {
     const int sms = qmoe::sm_count();
-    if (dict_smem && row_round_efficiency(a.m.rows, nt_max) >= 0.95) return launch_rows(a, nt_max, st);
+    if (dict_smem && use_row_kernel(a.m.rows, nt_max)) return launch_rows(a, nt_max, st);
     a.nt_max = nt_max;
     a.rows_per_tile = rows_per_tile;
     a.row_tiles = (a.m.rows + rows_per_tile - 1) / rows_per_tile;
@@ -2034,6 +2036,29 @@ extern "C" int qmoe_moe_layer_ws_size(int E, int d_model, int d_ff, int T, int k
     return QMOE_OK;
 }
 
+// launches with this many token slots stage the compact dictionary in shared memory; smaller
+// ones read it through L1/L2
+#ifndef QMOE_SMEM_DICT_MIN_SLOTS
+#define QMOE_SMEM_DICT_MIN_SLOTS 16
+#endif
+
+extern "C" int qmoe_moe_layer_kernels(int E, int d_model, int d_ff, int T, int k, int* wi_kernel, int* wo_kernel,
+                                      int* tc) {
+    qmoe::clear_error();
+    if (!wi_kernel || !wo_kernel || !tc || E < 1 || E > kPlanMaxE || d_model < 2 || d_ff < 2 || T < 0 || k < 1 ||
+        k > E)
+        return fail(QMOE_EINVAL, "qmoe_moe_layer_kernels: bad sizes or NULL outputs");
+    const long long slots = (long long)T * k;
+    const bool big = slots >= QMOE_SMEM_DICT_MIN_SLOTS;
+    const int budget = big ? kBudgetSmemDict : kBudgetGlobalDict;
+    const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);
+    if (!nt_wi || !nt_wo) return fail(QMOE_EUNSUPPORTED, "qmoe_moe_layer_kernels: d_model or d_ff too large");
+    *wi_kernel = !big ? QMOE_KERNEL_FLAT_L2 : use_row_kernel(d_ff, nt_wi) ? QMOE_KERNEL_ROWS : QMOE_KERNEL_FLAT;
+    *wo_kernel = !big ? QMOE_KERNEL_FLAT_L2 : use_row_kernel(d_model, nt_wo) ? QMOE_KERNEL_ROWS : QMOE_KERNEL_FLAT;
+    *tc = big && slots >= kTcMinSlots && d_model % 8 == 0 && d_ff % 8 == 0 ? 1 : 0;
+    return QMOE_OK;
+}
+
 extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, const qmoe_matrix_set* wo,
                               const void* x_bf16, int T, int k, const int32_t* ids, const float* gates, void* y,
                               int y_is_f32, void* workspace, size_t ws_bytes, void* stream) {
@@ -2049,11 +2074,8 @@ extern "C" int qmoe_moe_layer(const qmoe_dict* dict, const qmoe_matrix_set* wi, 
     MoeWs w = moe_ws_layout(workspace, E, d_model, d_ff, T, k);
     if (ws_bytes < w.bytes) return fail(QMOE_ECAPACITY, "qmoe_moe_layer: workspace too small");
     const long long slots = (long long)T * k;
-    // launches with this many token slots stage the compact dictionary in shared memory; smaller
-    // ones read it through L1/L2
-#ifndef QMOE_SMEM_DICT_MIN_SLOTS
-#define QMOE_SMEM_DICT_MIN_SLOTS 16
-#endif
+    // launches with at least QMOE_SMEM_DICT_MIN_SLOTS token slots stage the compact dictionary in
+    // shared memory; smaller ones read it through L1/L2
     const bool big = slots >= QMOE_SMEM_DICT_MIN_SLOTS;
     const int budget = big ? kBudgetSmemDict : kBudgetGlobalDict;
     const int nt_wi = nt_max_for(d_model, budget), nt_wo = nt_max_for(d_ff, budget);

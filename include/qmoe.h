@@ -272,6 +272,28 @@ int qmoe_moe_layer_ws_size(int E, int d_model, int d_ff, int T, int k,
                            size_t* bytes);
 
 /*
+ * Which dictionary kernel a qmoe_moe_layer call with these shapes launches for
+ * each of its two matrices (host only, no device work): QMOE_KERNEL_FLAT, the
+ * flat-stream CUDA-core kernel (a warp decodes a run of rows as one codeword
+ * stream; compact table in shared memory); QMOE_KERNEL_ROWS, the
+ * row-per-lane CUDA-core kernel (a lane walks one row; compact table in
+ * shared memory), taken when a job's rows fill the block's warps in nearly
+ * whole rounds; QMOE_KERNEL_FLAT_L2, the flat-stream kernel reading the
+ * compact table through L1/L2 (calls with fewer than 16 token slots).  *tc is
+ * 1 when the call also launches the tensor-core kernel for experts with at
+ * least 32 tokens (calls with at least 256 token slots).  Both CUDA-core
+ * kernels compute the same sums (QMoE page, "The GPU Decoding Kernel"); they
+ * differ in how work is spread.
+ * Errors: EINVAL (bad sizes or NULL outputs), EUNSUPPORTED (d_model or d_ff
+ * too large for the staged activations).
+ */
+#define QMOE_KERNEL_FLAT 0
+#define QMOE_KERNEL_ROWS 1
+#define QMOE_KERNEL_FLAT_L2 2
+int qmoe_moe_layer_kernels(int E, int d_model, int d_ff, int T, int k,
+                           int* wi_kernel, int* wo_kernel, int* tc);
+
+/*
  * Switch-Transformer-shaped MoE feed-forward layer on dictionary-coded
  * experts: for every token t and slot j with expert e = ids[t][j],
  *   h = bf16(relu(Wi_e x_t)),  o = Wo_e h,  y_t = sum_j gates[t][j] * o
