@@ -191,16 +191,16 @@ def test_c2048_full_shape_t4096(dev, c2048):
 
 
 def test_c2048_shaped_token_counts_around_tensor_core_threshold(dev):
-    """Six c2048-shaped experts (d_model 2080, d_ff 6144) with 31, 32, 33, 3, 150 and 7 tokens routed
-    by hand (T = 256, k = 1, enough slots for the tensor-core kernel): its threshold from both sides,
-    a 150-token expert split into several tensor-core jobs, several-token chunks with odd remainders
-    on the CUDA-core kernel (wi and wo token classes of the full-size layer)."""
+    """Six c2048-shaped experts (d_model 2080, d_ff 6144) with 31, 32, 33, 3, 300 and 7 tokens routed
+    by hand (T = 406, k = 1, enough slots for the tensor-core kernel): its threshold from both sides,
+    a 300-token expert split into two tensor-core jobs (at most 256 tokens each), several-token chunks
+    with odd remainders on the CUDA-core kernels (wi and wo token classes of the full-size layer)."""
     cfg = synth.SWITCH_C2048
     import dataclasses
     small = dataclasses.replace(cfg, E=6)
     layer = build_dict_layer(small, dev)
     experts = SeededExperts(small)
-    counts = [31, 32, 33, 3, 150, 7]
+    counts = [31, 32, 33, 3, 300, 7]
     rid = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(counts)])
     rid = rid[np.random.default_rng(5).permutation(rid.size)].reshape(-1, 1)
     rg = np.random.default_rng(6).uniform(0.2, 1.0, size=rid.shape)
