@@ -4,12 +4,12 @@
 One step = one pass of the dictionary-path hot path over one token batch of
 the switch-c2048-shaped MoE FFN layer (E=2048 experts, d_model=2080,
 d_ff=6144, ternary weights with P(0)=0.886 dictionary-coded: ~0.76 bits per
-weight of codewords, ~0.82 stored with row starts, block lengths and row
+weight of codewords, ~0.81 stored with row starts, block lengths and row
 scales; T=4096 bf16 tokens, top-1 Zipf(1.0) routing): route (top-1 + softmax
 gate) -> bucket tokens by expert -> fused decode-multiply of every touched
 expert's wi with ReLU -> fused decode-multiply of wo with the gate applied.
 Inputs are resident in HBM; each step streams the touched experts' compressed
-weights (about 2.6 GB, 20x the L2), so no L2 flush is needed.
+weights (about 2.5 GB, 20x the L2), so no L2 flush is needed.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
