@@ -146,6 +146,35 @@ def test_corrupt_stream_reports_format_error(dev, dict886):
     assert Q.qmoe_check_status() == Q.QMOE_OK          # the error word was cleared
 
 
+@pytest.mark.parametrize("which", ["wi", "wo"])
+def test_corrupt_stream_in_a_layer_call(dev, which):
+    """A codeword of expert 0 replaced by a 28-weight run (its block now expands past its end) in a
+    layer call that stages the table in shared memory: the row-per-lane kernel (wi, 512 rows) and the
+    flat-stream kernel (wo, 256 rows) both record QMOE_EFORMAT; their activation reads stay inside the
+    staged row and its zero padding."""
+    E, d, f, T, p0 = 2, 256, 512, 32, 0.886
+    assert Q.qmoe_moe_layer_kernels(E, d, f, T, 1)[:2] == (Q.QMOE_KERNEL_ROWS, Q.QMOE_KERNEL_FLAT)
+    wi = oracle_matrix_set(21, E, synth.WI, f, d, p0)
+    wo = oracle_matrix_set(21, E, synth.WO, d, f, p0)
+    lengths = C.expansion(dictionary(p0))[0]
+    tgt = wi if which == "wi" else wo
+    codes = tgt[0].copy()
+    i = int(np.argmax(lengths[codes[: int(tgt[1][1])]] < 28))      # inside expert 0's stream
+    codes[i] = int(np.argmax(lengths))
+    wi_codes, wo_codes = (codes, wo[0]) if which == "wi" else (wi[0], codes)
+    mwi = Q.MatrixSet.from_host(wi_codes, wi[2], wi[3], f, d, code_base=wi[1], count=E)
+    mwo = Q.MatrixSet.from_host(wo_codes, wo[2], wo[3], d, f, code_base=wo[1], count=E)
+    dd = Q.Dictionary(dictionary(p0))
+    x = bf16_tensor(synth.activations_bf16(21, T, d))
+    ids = torch.zeros((T, 1), dtype=torch.int32, device=dev)       # every token to expert 0
+    gates = torch.ones((T, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(Q.qmoe_moe_layer_ws_size(E, d, f, T, 1), dtype=torch.uint8, device=dev)
+    y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    Q.qmoe_moe_layer(dd, mwi, mwo, x, ids, gates, y, ws, y_is_f32=True)
+    assert Q.qmoe_check_status() == Q.QMOE_EFORMAT
+    assert Q.qmoe_check_status() == Q.QMOE_OK          # the error word was cleared
+
+
 def test_bad_arguments_rejected_on_host(dev, dict886):
     tern, codes, off, scale = oracle_matrix(9, 0, 0, 4, 64, 0.886)
     m = _single(codes, off, scale, 4, 64)
